@@ -1,0 +1,234 @@
+"""fp64 CPU oracle for the GQA decode step — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this package.  The CUDA library never links or calls
+it, and this package imports nothing from the CUDA library: the two meet only
+through the seeded inputs the tests generate.
+
+The arithmetic lives in ``gqa_oracle.c`` (plain C, fp64, plain loops); this
+module only builds it with gcc and marshals numpy arrays through ctypes.  The
+method it follows, with the passages it restates, is described in the C file's
+header: scaled dot-product attention per query head, query head h reading KV
+head floor(h / G), softmax over the valid cached tokens, optional FP8 E4M3
+cache values times a per-(sequence, KV head) scale.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import time
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+F16, BF16, E4M3, F64 = 0, 1, 2, 3
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with gcc -O2 (no fast-math) and OpenMP."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    vp, i32, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    lib.oracle_gqa_decode.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, f64, vp,
+                                      i32, i32, i32, i32, i32, i32]
+    lib.oracle_gqa_decode.restype = i32
+    lib.oracle_gqa_decode_rows.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, f64,
+                                           vp, i32, vp, i32, i32, i32, i32, i32,
+                                           i32]
+    lib.oracle_gqa_decode_rows.restype = i32
+    lib.oracle_gqa_weights.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, f64,
+                                       i32, i32, vp, vp, i32, i32, i32, i32, i32]
+    lib.oracle_gqa_weights.restype = i32
+    lib.oracle_kv_bytes_per_token.argtypes = [i32, i32, i32, i32]
+    lib.oracle_kv_bytes_per_token.restype = ctypes.c_uint64
+    lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_f64.restype = f64
+    lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f64.restype = f64
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f64.restype = f64
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = i32
+    _lib = lib
+    return lib
+
+
+# --------------------------------------------------------------- marshalling
+
+def _as_raw(x, what):
+    """numpy/torch CPU array -> (contiguous numpy array, element type code).
+
+    16-bit floats travel as their raw bit patterns (uint16) and FP8 as raw
+    bytes (uint8); the oracle decodes them itself.
+    """
+    try:  # accept torch CPU tensors without making torch a hard dependency
+        import torch
+        if isinstance(x, torch.Tensor):
+            if x.is_cuda:
+                raise ValueError(f"{what}: the oracle takes host tensors only")
+            x = x.contiguous()
+            if x.dtype == torch.float16:
+                return x.view(torch.uint16).numpy(), F16
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.uint16).numpy(), BF16
+            if x.dtype == torch.float8_e4m3fn:
+                return x.view(torch.uint8).numpy(), E4M3
+            if x.dtype == torch.uint8:
+                return x.numpy(), E4M3
+            x = x.double().numpy()
+    except ImportError:
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16:
+        return x.view(np.uint16), F16
+    if x.dtype == np.uint8:
+        return x, E4M3
+    return np.ascontiguousarray(x, dtype=np.float64), F64
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _scales(s):
+    if s is None:
+        return None
+    try:
+        import torch
+        if isinstance(s, torch.Tensor):
+            s = s.double().numpy()
+    except ImportError:
+        pass
+    return np.ascontiguousarray(s, dtype=np.float64)
+
+
+def _lens(seq_lens):
+    try:
+        import torch
+        if isinstance(seq_lens, torch.Tensor):
+            seq_lens = seq_lens.cpu().numpy()
+    except ImportError:
+        pass
+    return np.ascontiguousarray(seq_lens, dtype=np.int32)
+
+
+def gqa_decode(q, k, v, seq_lens, scale, *, k_scale=None, v_scale=None,
+               nthreads: int = 0) -> np.ndarray:
+    """out[B, Hq, D] (float64) of one GQA decode step.
+
+    q: [B, Hq, D]; k, v: [B, Hkv, Smax, D] (float16/bfloat16/float64 values, or
+    FP8 E4M3 bytes with ``k_scale``/``v_scale`` of shape [B, Hkv]);
+    seq_lens: [B] valid cached tokens per sequence.
+    """
+    lib = _load()
+    qa, qt = _as_raw(q, "q")
+    ka, kt = _as_raw(k, "k")
+    va, vt = _as_raw(v, "v")
+    if kt != vt:
+        raise ValueError("k and v must share an element type")
+    B, Hq, D = qa.shape
+    _, Hkv, Smax, D2 = ka.shape
+    if D2 != D or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    lens = _lens(seq_lens)
+    ks, vs = _scales(k_scale), _scales(v_scale)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    rc = lib.oracle_gqa_decode(_ptr(qa), qt, _ptr(ka), _ptr(va), kt, _ptr(ks),
+                               _ptr(vs), _ptr(lens), float(scale), _ptr(out),
+                               B, Hq, Hkv, Smax, D, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gqa_decode rejected its arguments")
+    return out
+
+
+def gqa_decode_rows(q, k, v, seq_lens, scale, bh, *, k_scale=None,
+                    v_scale=None, nthreads: int = 0) -> np.ndarray:
+    """Output rows [n, D] (float64) for the (b, h) pairs in ``bh`` ([n, 2])."""
+    lib = _load()
+    qa, qt = _as_raw(q, "q")
+    ka, kt = _as_raw(k, "k")
+    va, vt = _as_raw(v, "v")
+    B, Hq, D = qa.shape
+    _, Hkv, Smax, _ = ka.shape
+    pairs = np.ascontiguousarray(np.asarray(bh, dtype=np.int32).reshape(-1, 2))
+    n = pairs.shape[0]
+    lens = _lens(seq_lens)
+    ks, vs = _scales(k_scale), _scales(v_scale)
+    out = np.zeros((n, D), dtype=np.float64)
+    rc = lib.oracle_gqa_decode_rows(_ptr(qa), qt, _ptr(ka), _ptr(va), kt,
+                                    _ptr(ks), _ptr(vs), _ptr(lens), float(scale),
+                                    _ptr(pairs), n, _ptr(out), B, Hq, Hkv, Smax,
+                                    D, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gqa_decode_rows rejected its arguments")
+    return out
+
+
+def gqa_weights(q, k, v, seq_lens, scale, b, h, *, k_scale=None,
+                v_scale=None):
+    """(weights[L], out_row[D]) of one (b, h) row: the debug entry."""
+    lib = _load()
+    qa, qt = _as_raw(q, "q")
+    ka, kt = _as_raw(k, "k")
+    va, _ = _as_raw(v, "v")
+    B, Hq, D = qa.shape
+    _, Hkv, Smax, _ = ka.shape
+    lens = _lens(seq_lens)
+    ks, vs = _scales(k_scale), _scales(v_scale)
+    w = np.zeros(Smax, dtype=np.float64)
+    row = np.zeros(D, dtype=np.float64)
+    L = lib.oracle_gqa_weights(_ptr(qa), qt, _ptr(ka), _ptr(va), kt, _ptr(ks),
+                               _ptr(vs), _ptr(lens), float(scale), int(b), int(h),
+                               _ptr(w), _ptr(row), B, Hq, Hkv, Smax, D)
+    if L < 0:
+        raise ValueError("oracle_gqa_weights rejected its arguments")
+    return w[:L].copy(), row
+
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
+                       bytes_per_elem: int) -> int:
+    return int(_load().oracle_kv_bytes_per_token(layers, kv_heads, head_dim,
+                                                 bytes_per_elem))
+
+
+def f16_to_f64(bits: int) -> float:
+    return _load().oracle_f16_to_f64(bits)
+
+
+def bf16_to_f64(bits: int) -> float:
+    return _load().oracle_bf16_to_f64(bits)
+
+
+def e4m3_to_f64(bits: int) -> float:
+    return _load().oracle_e4m3_to_f64(bits)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def timed_decode(*args, **kwargs):
+    """(out, seconds) of gqa_decode, wall clock, for the CPU baseline."""
+    t0 = time.perf_counter()
+    out = gqa_decode(*args, **kwargs)
+    return out, time.perf_counter() - t0
