@@ -1,0 +1,343 @@
+#!/usr/bin/env python3
+"""Benchmark of the GQA decode step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step = one gqa_decode call over the whole batch of the workload (default:
+the Llama-2/3-70B-shaped long-context decode, B=8, Hq=64, Hkv=8, D=128,
+seq_len=8192, bf16).  Inputs are synthetic, seeded, and resident in HBM when
+the timed region starts; they exceed the 126 MB L2 (268 MB for the default
+workload) and the kernel loads K/V with an L2 evict-first hint, so nothing is
+flushed between steps.  Each step is bracketed by CUDA events recorded on the
+launching stream; the timed region is bracketed by a barrier and
+torch.cuda.synchronize() on both sides.
+
+Printed (rank 0, one JSON line): the metric (us/step, lower is better), KV
+GB/s and the HBM roofline fraction, an end-to-end figure through the public
+API with host buffers (pinned H2D of the step's inputs + decode + D2H of the
+output), SM clocks sampled during the timed region, and the fp64 CPU oracle
+timed on a bounded sample of the same workload (``cpu_baseline``).
+
+``--impl reference`` times only that oracle (the reference arm): each step is
+a bounded sample of the workload, extrapolated to the metric's unit.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(the decode step has no exchange between GPUs); rank 0 reports the maximum
+step time over ranks and the aggregate KV bandwidth.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("GQA decode attention µs/step, KV-cache GB/s and % of B300 HBM "
+          "peak (1 GPU)")
+FALLBACK_HBM_GBS = 6400.0
+SPEC_HBM_GBS = 8000.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.rows = []
+        self.gpu_index = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}",
+                 f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                self.rows.append(parts)
+
+    def summary(self):
+        if not self.rows:
+            return None
+        sm = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in self.rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def cpu_baseline(w, inp, budget_s: float = 10.0):
+    """fp64 oracle on the host cores: whole sequences, one at a time, until
+    ``budget_s`` has passed; extrapolated to one full step (us/step)."""
+    import numpy as np
+    import oracle
+    import torch
+    oracle.build()
+    threads = oracle.max_threads()
+    lens = inp["seq_lens"]
+    done_tokens = 0
+    total_tokens = int(lens.sum())
+    t0 = time.perf_counter()
+    n_seq = 0
+    order = list(range(w.B))
+    for b in order:
+        sl = slice(b, b + 1)
+        ks = inp["k_scale"][sl] if inp["k_scale"] is not None else None
+        vs = inp["v_scale"][sl] if inp["v_scale"] is not None else None
+        oracle.gqa_decode(inp["q"][sl], inp["k"][sl], inp["v"][sl], lens[sl],
+                          inp["scale"], k_scale=ks, v_scale=vs,
+                          nthreads=threads)
+        done_tokens += int(lens[b])
+        n_seq += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    frac = done_tokens / total_tokens if total_tokens else 1.0
+    us_per_step = el / frac * 1e6 if frac > 0 else el * 1e6
+    return {"value": us_per_step, "unit": "us/step", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"{n_seq} of {w.B} sequences ({done_tokens} of "
+                       f"{total_tokens} tokens, all {w.Hq} query heads), fp64 "
+                       f"C oracle, {el:.2f} s wall, extrapolated by tokens")}
+
+
+# ------------------------------------------------------------------ runner
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    a = ap.parse_args(argv)
+
+    from grouped_query_attention_11_b300.workloads import (HEADLINE,
+                                                           WORKLOADS,
+                                                           make_inputs)
+    name = a.workload or HEADLINE
+    w = WORKLOADS[name]
+    ws, rank, local = dist_env()
+    peak, peak_kind = load_peaks()
+    cfg = {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "G": w.G,
+           "D": w.D, "seq_len": (w.Smax if w.lens[0] == "uniform" else
+                                 f"uniform[{w.lens[1]},{w.lens[2]}]"),
+           "Smax": w.Smax, "qo_dtype": w.dtype,
+           "kv_dtype": "e4m3" if w.kv == "e4m3" else w.dtype,
+           "l2": "inputs larger than L2, K/V loaded evict-first; no flush",
+           "parallelism": "replicas" if a.gpus > 1 else "single"}
+    warmup = max(3, a.warmup)
+
+    if a.impl == "reference":
+        if rank != 0:
+            return 0
+        inp = make_inputs(w, pad="zero")
+        # Each step is a bounded sample (about 10 s of oracle work); at most
+        # ~60 s in all, whatever --steps asks for.
+        n_steps = max(1, min(a.steps, 6))
+        budget = max(2.0, 60.0 / n_steps)
+        vals = []
+        last = None
+        for _ in range(n_steps):
+            last = cpu_baseline(w, inp, budget_s=budget)
+            vals.append(last["value"])
+        v = statistics.median(vals)
+        line = {"metric": METRIC, "value": v, "unit": "us/step",
+                "impl": "reference", "n_gpus": a.gpus, "steps": len(vals),
+                "warmup": 0, "ms_per_step": v / 1e3, "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfg,
+                "cpu_baseline": dict(last, value=v),
+                "e2e": {"value": v, "unit": "us/step",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import grouped_query_attention_11_b300 as gq
+
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gq.lib()
+
+    inp = make_inputs(w, pad="zero", seed=w.seed + rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
+         for k, v in inp.items()}
+    out = torch.empty_like(d["q"])
+    stream = torch.cuda.current_stream()
+
+    def step(o=out):
+        return gq.decode_inputs(d, out=o, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    assert gq.gqa_device_errors(stream) == 0
+
+    algo_bytes = w.algorithmic_bytes(inp["seq_lens"])
+    K = a.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3 if sampler and sampler.proc else 0)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        launches += gq.gqa_last_launch_count()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if ws > 1:
+        torch.distributed.barrier()
+    if sampler:
+        sampler.stop()
+    assert gq.gqa_device_errors(stream) == 0
+
+    per = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]  # us
+    us = statistics.mean(per)
+    us_med = statistics.median(per)
+    if ws > 1:
+        t = torch.tensor([us], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        us_max = float(t.item())
+    else:
+        us_max = us
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    ek = max(1, a.e2e_steps)
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v)
+            for k, v in inp.items()}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values()
+              if isinstance(v, torch.Tensor))
+    d2h = h_out.numel() * h_out.element_size()
+    dd = {k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor)
+              else v) for k, v in host.items()}
+
+    def e2e_step():
+        for k, v in host.items():
+            if isinstance(v, torch.Tensor):
+                dd[k].copy_(v, non_blocking=True)
+        gq.decode_inputs(dd, out=out, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    es.record(stream)
+    for _ in range(ek):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = es.elapsed_time(ee) * 1e3 / ek
+    if ws > 1:
+        t = torch.tensor([e2e_us], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_us = float(t.item())
+    e2e = {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": ek}
+    del dd
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    achieved = algo_bytes / (us * 1e-6) / 1e9
+    clocks = sampler.summary() if sampler else None
+    cpu = None
+    if not a.no_cpu_baseline and ws == 1:
+        cpu = cpu_baseline(w, inp, budget_s=10.0)
+    line = {
+        "metric": METRIC, "value": us_max, "unit": "us/step",
+        "n_gpus": ws, "steps": K, "warmup": warmup,
+        "ms_per_step": us_max / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
+        w.kv != "e4m3" else "e4m3 KV / bf16 q,out", "data": "synthetic",
+        "config": cfg,
+        "kv_gbs": achieved * ws, "hbm_frac_of_" + peak_kind: achieved / peak,
+        "hbm_frac_of_spec_8tbs": achieved / SPEC_HBM_GBS,
+        "us_per_step_median": us_med, "wall_s_timed_region": t_wall,
+        "algorithmic_bytes_per_step": algo_bytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "traffic": None},
+        "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,196 @@
+"""Python binding of libgqa_b300.so, the B300 GQA decode library.
+
+Argument marshalling only: every step of the decode runs in the library's CUDA
+kernels.  torch supplies device memory and the stream; nothing here computes
+attention, and there is no fallback — if the library is missing or a call
+fails, an exception is raised.
+
+The C interface (``include/gqa.h``) is the contract; the functions below keep
+its names:
+
+* :func:`gqa_decode` — one decode step with a float16 / bfloat16 cache;
+* :func:`gqa_decode_fp8` — the same with an FP8 E4M3 cache and per-(sequence,
+  KV head) scales;
+* :func:`gqa_kv_bytes_per_token`, :func:`gqa_status_string`,
+  :func:`gqa_device_errors`, :func:`gqa_set_num_ctas`,
+  :func:`gqa_last_launch_count`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgqa_b300.so")
+
+GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, \
+    GQA_ERR_DEVICE = 0, 1, 2, 3, 4
+GQA_F16, GQA_BF16, GQA_E4M3 = 0, 1, 2
+
+# Every function include/gqa.h declares, with its ctypes signature.
+_VP, _I32, _F32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "gqa_decode": (_I32, [_VP, _VP, _VP, _VP, _F32, _VP, _I32, _I32, _I32,
+                          _I32, _I32, _I32, _VP]),
+    "gqa_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
+                              _I32, _I32, _I32, _I32, _I32, _VP]),
+    "gqa_kv_bytes_per_token": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
+    "gqa_status_string": (ctypes.c_char_p, [_I32]),
+    "gqa_device_errors": (_I32, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
+    "gqa_set_num_ctas": (None, [_I32]),
+    "gqa_last_launch_count": (_I32, []),
+}
+
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {gqa_status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m grouped_query_attention_11_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def gqa_status_string(status: int) -> str:
+    return lib().gqa_status_string(int(status)).decode()
+
+
+def gqa_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
+                           bytes_per_elem: int) -> int:
+    return int(lib().gqa_kv_bytes_per_token(layers, kv_heads, head_dim,
+                                            bytes_per_elem))
+
+
+def gqa_set_num_ctas(n: int) -> None:
+    lib().gqa_set_num_ctas(int(n))
+
+
+def gqa_last_launch_count() -> int:
+    return int(lib().gqa_last_launch_count())
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def gqa_device_errors(stream=None) -> int:
+    """Synchronises the stream; returns and clears the kernels' fault flags."""
+    flags = ctypes.c_uint32(0)
+    st = lib().gqa_device_errors(_stream_handle(stream), ctypes.byref(flags))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_device_errors")
+    return int(flags.value)
+
+
+# ------------------------------------------------------------ torch helpers
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return GQA_F16
+    if t.dtype == torch.bfloat16:
+        return GQA_BF16
+    raise TypeError(f"q/out must be float16 or bfloat16, got {t.dtype}")
+
+
+def _check_dev(name, t):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out=None,
+               stream=None):
+    """One GQA decode step; returns ``out`` [B, Hq, D].
+
+    q [B, Hq, D], k_cache / v_cache [B, Hkv, Smax, D] (same 16-bit dtype as
+    q), seq_lens [B] int32 — all CUDA tensors on the current device.
+    """
+    import torch
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("seq_lens", seq_lens)):
+        _check_dev(n, t)
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, k_cache and v_cache must share a dtype")
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    B, Hq, D = q.shape
+    _, Hkv, Smax, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_dev("out", out)
+    st = lib().gqa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                          seq_lens.data_ptr(), float(scale), out.data_ptr(),
+                          B, Hq, Hkv, Smax, D, _dtype_code(q),
+                          _stream_handle(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_decode")
+    return out
+
+
+def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens,
+                   scale: float, out=None, stream=None):
+    """GQA decode step over an FP8 E4M3 cache; returns ``out`` [B, Hq, D].
+
+    k_cache / v_cache [B, Hkv, Smax, D] float8_e4m3fn (or uint8 codes),
+    k_scale / v_scale [B, Hkv] float32; other arguments as gqa_decode.
+    """
+    import torch
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("k_scale", k_scale), ("v_scale", v_scale),
+                 ("seq_lens", seq_lens)):
+        _check_dev(n, t)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{n} must be float8_e4m3fn, got {t.dtype}")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("k_scale / v_scale must be float32")
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    B, Hq, D = q.shape
+    _, Hkv, Smax, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_dev("out", out)
+    st = lib().gqa_decode_fp8(q.data_ptr(), k_cache.data_ptr(),
+                              v_cache.data_ptr(), k_scale.data_ptr(),
+                              v_scale.data_ptr(), seq_lens.data_ptr(),
+                              float(scale), out.data_ptr(), B, Hq, Hkv, Smax,
+                              D, _dtype_code(q), _stream_handle(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_decode_fp8")
+    return out
+
+
+def decode_inputs(inp: dict, out=None, stream=None):
+    """Runs the right entry point on a dict of CUDA tensors (the layout the
+    input generator produces, moved to the device)."""
+    if inp.get("k_scale") is not None:
+        return gqa_decode_fp8(inp["q"], inp["k"], inp["v"], inp["k_scale"],
+                              inp["v_scale"], inp["seq_lens"], inp["scale"],
+                              out=out, stream=stream)
+    return gqa_decode(inp["q"], inp["k"], inp["v"], inp["seq_lens"],
+                      inp["scale"], out=out, stream=stream)

@@ -1,0 +1,351 @@
+// gqa_api.cu — host side of libgqa_b300.so: the C ABI declared in
+// include/gqa.h (argument checks, TMA descriptors, per-stream scratch,
+// kernel selection and launch).  All GPU work is in gqa_decode_kernel.cuh.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gqa.h"
+#include "gqa_decode_kernel.cuh"
+
+namespace gqa {
+namespace {
+
+// ------------------------------------------------------------ driver entry
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// Rank-3 view [B*Hkv][Smax][D] of a cache, box = one pipeline tile.
+bool make_cache_map(CUtensorMap* map, const void* base, int elem_bytes,
+                    int B, int Hkv, int Smax, int D) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const int box_elems = (elem_bytes == 1) ? D : 64;
+  const int box_bytes = box_elems * elem_bytes;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(Smax),
+                        static_cast<cuuint64_t>(B) * Hkv};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem_bytes,
+                           static_cast<cuuint64_t>(Smax) * D * elem_bytes};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_elems),
+                       static_cast<cuuint32_t>(kTileTokens), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapSwizzle sw = box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                 : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = enc(
+      map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                           : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+      3, const_cast<void*>(base), dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------- kernel table
+
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap,
+                          const DecodeParams);
+
+struct Variant {
+  KernelFn fn;
+  int smem;
+};
+
+template <int KV, bool QB, int D, int HB>
+Variant variant() {
+  return {&gqa_decode_kernel<KV, QB, D, HB>, Cfg<KV, D, HB>::kSmemBytes};
+}
+
+template <int KV, bool QB, int D>
+Variant pick_hb(int hb) {
+  switch (hb) {
+    case 1: return variant<KV, QB, D, 1>();
+    case 2: return variant<KV, QB, D, 2>();
+    default: return variant<KV, QB, D, 4>();
+  }
+}
+
+template <int KV, bool QB>
+Variant pick_d(int D, int hb) {
+  return D == 64 ? pick_hb<KV, QB, 64>(hb) : pick_hb<KV, QB, 128>(hb);
+}
+
+Variant pick(int kv, bool q_bf16, int D, int hb) {
+  if (kv == kKvF16) return pick_d<kKvF16, false>(D, hb);
+  if (kv == kKvBF16) return pick_d<kKvBF16, true>(D, hb);
+  return q_bf16 ? pick_d<kKvE4M3, true>(D, hb) : pick_d<kKvE4M3, false>(D, hb);
+}
+
+// ------------------------------------------------------- per-device state
+
+std::mutex g_mu;
+
+struct DeviceInfo {
+  int sms = 0;
+  std::map<KernelFn, int> blocks_per_sm;  // configured variants
+};
+std::map<int, DeviceInfo> g_dev;
+
+// Scratch per (device, stream): [error flags | counters | lse | partial O].
+struct Scratch {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+
+int g_num_ctas_override = 0;
+thread_local int t_last_launches = 0;
+
+constexpr size_t kHeaderBytes = 256;  // error word(s)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+cudaError_t configure(int dev, const Variant& v, int* sms, int* per_sm) {
+  DeviceInfo& di = g_dev[dev];
+  if (di.sms == 0) {
+    cudaError_t e =
+        cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  auto it = di.blocks_per_sm.find(v.fn);
+  if (it == di.blocks_per_sm.end()) {
+    cudaError_t e = cudaFuncSetAttribute(
+        v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, v.fn, kThreads,
+                                                      v.smem);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    it = di.blocks_per_sm.emplace(v.fn, n).first;
+  }
+  *sms = di.sms;
+  *per_sm = it->second;
+  return cudaSuccess;
+}
+
+cudaError_t scratch_for(int dev, cudaStream_t stream, size_t need,
+                        void** out) {
+  Scratch& s = g_scratch[{dev, stream}];
+  if (s.bytes < need) {
+    if (s.ptr) {
+      cudaError_t e = cudaFreeAsync(s.ptr, stream);
+      s.ptr = nullptr;
+      s.bytes = 0;
+      if (e != cudaSuccess) return e;
+    }
+    const size_t bytes = align_up(need + need / 4, 1 << 20);
+    cudaError_t e = cudaMallocAsync(&s.ptr, bytes, stream);
+    if (e != cudaSuccess) {
+      s.ptr = nullptr;
+      return e;
+    }
+    // error flags and counters start (and stay, between calls) at zero;
+    // partials need no initial value.
+    e = cudaMemsetAsync(s.ptr, 0, bytes, stream);
+    if (e != cudaSuccess) return e;
+    s.bytes = bytes;
+  }
+  *out = s.ptr;
+  return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+gqa_status check_common(const void* q, const void* k, const void* v,
+                        const int32_t* seq_lens, float scale, const void* out,
+                        int B, int Hq, int Hkv, int Smax, int D) {
+  if (!q || !k || !v || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(out, 16) || !aligned(seq_lens, 4))
+    return GQA_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Smax < 1 || D < 1)
+    return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+  // TMA coordinates and the unit index are 32-bit.
+  if (static_cast<long long>(B) * Hq > INT32_MAX) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+gqa_status launch(const void* q, const void* k, const void* v,
+                  const float* k_scale, const float* v_scale,
+                  const int32_t* seq_lens, float scale, void* out, int B,
+                  int Hq, int Hkv, int Smax, int D, int kv_kind, bool q_bf16,
+                  void* stream_ptr) {
+  t_last_launches = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int G = Hq / Hkv;
+  const int NHC = (G + kMaxUnitRows - 1) / kMaxUnitRows;
+  const int R = (G + NHC - 1) / NHC;
+  const int hb = R <= 16 ? 1 : (R <= 32 ? 2 : 4);
+  const int rows_pad = hb * 16;
+  const long long units = static_cast<long long>(B) * Hkv * NHC;
+  if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
+
+  const Variant var = pick(kv_kind, q_bf16, D, hb);
+  const int elem_bytes = kv_kind == kKvE4M3 ? 1 : 2;
+
+  CUtensorMap map_k, map_v;
+  if (!make_cache_map(&map_k, k, elem_bytes, B, Hkv, Smax, D) ||
+      !make_cache_map(&map_v, v, elem_bytes, B, Hkv, Smax, D))
+    return GQA_ERR_CUDA;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  int sms = 0, per_sm = 0;
+  if (configure(dev, var, &sms, &per_sm) != cudaSuccess) return GQA_ERR_CUDA;
+  const int grid =
+      g_num_ctas_override > 0 ? g_num_ctas_override : sms * per_sm;
+
+  const size_t slots = static_cast<size_t>(grid) + static_cast<size_t>(units);
+  const size_t cnt_bytes = align_up(static_cast<size_t>(units) * 4, 256);
+  const size_t lse_bytes = align_up(slots * rows_pad * 4, 256);
+  const size_t o_bytes = slots * rows_pad * static_cast<size_t>(D) * 4;
+  void* ws = nullptr;
+  if (scratch_for(dev, stream, kHeaderBytes + cnt_bytes + lse_bytes + o_bytes,
+                  &ws) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+
+  DecodeParams p;
+  p.q = q;
+  p.out = out;
+  p.seq_lens = seq_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.error = reinterpret_cast<uint32_t*>(wb);
+  p.counters = reinterpret_cast<uint32_t*>(wb + kHeaderBytes);
+  p.part_lse = reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes);
+  p.part_o =
+      reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes + lse_bytes);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Smax = Smax;
+  p.G = G;
+  p.NHC = NHC;
+  p.R = R;
+
+  var.fn<<<grid, kThreads, var.smem, stream>>>(map_k, map_v, p);
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  t_last_launches = 1;
+  return GQA_OK;
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+gqa_status gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* seq_lens, float scale, void* out, int B,
+                      int Hq, int Hkv, int Smax, int D, gqa_dtype dtype,
+                      void* stream) {
+  gqa::t_last_launches = 0;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  const gqa_status st = gqa::check_common(q, k_cache, v_cache, seq_lens, scale,
+                                          out, B, Hq, Hkv, Smax, D);
+  if (st != GQA_OK) return st;
+  try {
+    return gqa::launch(q, k_cache, v_cache, nullptr, nullptr, seq_lens, scale,
+                       out, B, Hq, Hkv, Smax, D,
+                       dtype == GQA_BF16 ? gqa::kKvBF16 : gqa::kKvF16,
+                       dtype == GQA_BF16, stream);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
+}
+
+gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
+                          const void* v_cache, const float* k_scale,
+                          const float* v_scale, const int32_t* seq_lens,
+                          float scale, void* out, int B, int Hq, int Hkv,
+                          int Smax, int D, gqa_dtype qo_dtype, void* stream) {
+  gqa::t_last_launches = 0;
+  if (qo_dtype != GQA_F16 && qo_dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (!k_scale || !v_scale || !gqa::aligned(k_scale, 4) ||
+      !gqa::aligned(v_scale, 4))
+    return GQA_ERR_INVALID_ARG;
+  const gqa_status st = gqa::check_common(q, k_cache, v_cache, seq_lens, scale,
+                                          out, B, Hq, Hkv, Smax, D);
+  if (st != GQA_OK) return st;
+  try {
+    return gqa::launch(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale,
+                       out, B, Hq, Hkv, Smax, D, gqa::kKvE4M3,
+                       qo_dtype == GQA_BF16, stream);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
+}
+
+size_t gqa_kv_bytes_per_token(int layers, int kv_heads, int head_dim,
+                              int bytes_per_elem) {
+  if (layers <= 0 || kv_heads <= 0 || head_dim <= 0 || bytes_per_elem <= 0)
+    return 0;
+  return static_cast<size_t>(2) * static_cast<size_t>(layers) *
+         static_cast<size_t>(kv_heads) * static_cast<size_t>(head_dim) *
+         static_cast<size_t>(bytes_per_elem);
+}
+
+const char* gqa_status_string(gqa_status status) {
+  switch (status) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GQA_ERR_CUDA: return "CUDA error";
+    case GQA_ERR_DEVICE: return "device-side fault reported by a kernel";
+  }
+  return "unknown status";
+}
+
+gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
+  if (!flags) return GQA_ERR_INVALID_ARG;
+  *flags = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(gqa::g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  auto it = gqa::g_scratch.find({dev, stream});
+  if (it == gqa::g_scratch.end() || !it->second.ptr) return GQA_OK;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, it->second.ptr, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (v != 0 && cudaMemset(it->second.ptr, 0, 4) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  *flags = v;
+  return GQA_OK;
+}
+
+void gqa_set_num_ctas(int num_ctas) {
+  std::lock_guard<std::mutex> lock(gqa::g_mu);
+  gqa::g_num_ctas_override = num_ctas > 0 ? num_ctas : 0;
+}
+
+int gqa_last_launch_count(void) { return gqa::t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,766 @@
+// gqa_decode_kernel.cuh — the split-sequence GQA decode kernel for sm_103a.
+//
+// What one launch computes: for every sequence b, KV head j and query head h
+// of j's group (h = j*G .. j*G+G-1), softmax(scale * q[b,h] . K[b,j,t]) over
+// the t < seq_lens[b] cached tokens, applied to V[b,j,t] ("Grouped Query
+// Attention (GQA): Efficient Multi-Head Attention", Worked example 2 and Two
+// extremes; the head-to-KV-head mapping of "Llama-2 70B uses 64 query heads
+// ...", What the choice does to attention).
+//
+// How (design for B300, not taken from the pages):
+//
+//  * Work units.  A unit is (sequence b, KV head j, chunk of <= 64 query heads
+//    of j's group).  Its tokens are cut into 64-token tiles.  All tiles of all
+//    units form one flat list (sequence-major), computed on the device from
+//    seq_lens by every block: no host sync, ragged lengths cost nothing extra.
+//  * Persistent blocks.  The grid is one wave of blocks; block c takes the
+//    contiguous tile range [c*N/P, (c+1)*N/P).  Every block streams the same
+//    number of KV bytes (+-1 tile), whatever the length mix.  A unit cut by a
+//    range boundary is finished by the fused split combine below.
+//  * KV stream.  One producer warp issues TMA tensor loads (128-byte
+//    swizzle, L2 evict-first) of the K and V tiles into a multi-stage shared
+//    memory ring guarded by mbarriers.  Each KV byte is read from HBM once and
+//    serves all query heads of its group from shared memory.
+//  * Group-batched math.  Four consumer warps hold the group's query rows as
+//    mma A fragments (16 rows per head block; G < 16 pads with zero rows) and
+//    run QK^T and PV through mma.sync m16n8k16 with fp32 accumulation.  The
+//    online softmax (running row max, rescale, row sum) lives in registers;
+//    row reductions are two quad shuffles.
+//  * FP8 E4M3 cache.  Bytes are turned into exact f16 pairs in registers
+//    (cvt.rn.f16x2.e4m3x2); q is moved into f16 with a per-head-block power
+//    of two so no value can overflow; k_scale and the power of two fold into
+//    the score multiplier and v_scale into the output.
+//  * Split combine.  Warps of a block merge through shared memory.  A unit
+//    covered by one block is written out directly; otherwise each block
+//    writes a normalised partial (O, log2-sum-exp) and bumps a per-unit
+//    counter; the block that arrives last merges all partials of the unit and
+//    writes the output, then resets the counter.  No block ever waits on
+//    another block.
+//  * Every mbarrier wait gives up after a time limit, sets an error flag the
+//    host can query, and lets the block finish without hanging the GPU.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdint>
+#include <type_traits>
+
+#include "ptx.cuh"
+
+namespace gqa {
+
+constexpr int kTileTokens = 64;   // tokens per pipeline stage
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxUnitRows = 64;  // query heads per unit (4 head blocks)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
+constexpr int kSmemBudget = 200 * 1024;
+
+enum KvKind : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
+
+enum ErrorBits : uint32_t { kErrWaitTimeout = 1u };
+
+struct DecodeParams {
+  const void* q;            // [B, Hq, D] f16 / bf16
+  void* out;                // [B, Hq, D] same dtype as q
+  const int32_t* seq_lens;  // [B]
+  const float* k_scale;     // [B, Hkv] (E4M3 only)
+  const float* v_scale;     // [B, Hkv] (E4M3 only)
+  float* part_o;            // [slots, rows_pad, D]  normalised partial outputs
+  float* part_lse;          // [slots, rows_pad]     log2-sum-exp of partials
+  uint32_t* counters;       // [units] arrivals per unit (zero between calls)
+  uint32_t* error;          // fault flags
+  float scale_log2;         // softmax scale * log2(e)
+  int B, Hq, Hkv, Smax, G;
+  int NHC;                  // head chunks per KV head
+  int R;                    // query heads per head chunk (<= 64)
+};
+
+// ------------------------------------------------------------ compile-time
+
+template <int KV, int D, int HB>
+struct Cfg {
+  static constexpr int kElemBytes = (KV == kKvE4M3) ? 1 : 2;
+  static constexpr int kRowBytes = D * kElemBytes;            // one token
+  static constexpr int kTileBytes = kTileTokens * kRowBytes;  // K or V tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  // TMA box: 128-byte rows for 16-bit (D=128 needs two boxes), the whole row
+  // for E4M3 (128 B at D=128 -> 128B swizzle, 64 B at D=64 -> 64B swizzle).
+  static constexpr int kBoxElems = (KV == kKvE4M3) ? D : 64;
+  static constexpr int kBoxBytes = kTileTokens * kBoxElems * kElemBytes;
+  static constexpr int kBoxesPerTile = D / kBoxElems;
+  static constexpr int kWarpsPerBlock = kConsumerWarps / HB;  // per head block
+  static constexpr int kWarpTokens = kTileTokens / kWarpsPerBlock;
+  static constexpr int kSTiles = kWarpTokens / 8;   // S n-tiles per warp
+  static constexpr int kPSteps = kWarpTokens / 16;  // PV k-steps per warp
+  static constexpr int kOTiles = D / 8;             // O n-tiles
+  static constexpr int kQSteps = D / 16;            // QK k-steps
+  static constexpr int kRowsPad = HB * 16;
+  static constexpr int kMergeBytes =
+      kConsumerWarps * 16 * D * 4 + 2 * kConsumerWarps * 16 * 4;
+  static constexpr int kStagesRaw = (kSmemBudget - kMergeBytes - 1024) /
+                                    kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kRingBytes +
+                                    kMergeBytes + 2 * kStages * 8 + 64;
+  static_assert(kStages >= 2, "pipeline needs at least two stages");
+  static_assert(kSTiles % 2 == 0 && kPSteps >= 1, "warp tile shape");
+};
+
+__device__ __forceinline__ int clamp_len(int L, int Smax) {
+  return L < 0 ? 0 : (L > Smax ? Smax : L);
+}
+
+__device__ __forceinline__ int tiles_of(int L) {
+  return (L + kTileTokens - 1) / kTileTokens;
+}
+
+// Position of a block in the flat tile list, advanced one tile at a time.
+struct TileWalk {
+  int b;          // sequence
+  int L;          // its valid length
+  int nt;         // its tiles per unit
+  int j;          // unit within the sequence: kv_head * NHC + head_chunk
+  int ti;         // tile within the unit
+  long long pref; // global index of the sequence's first tile
+
+  __device__ __forceinline__ void next(const DecodeParams& p, int HU) {
+    if (++ti < nt) return;
+    ti = 0;
+    if (++j < HU) return;
+    j = 0;
+    pref += static_cast<long long>(nt) * HU;
+    do {
+      ++b;
+      if (b >= p.B) return;
+      L = clamp_len(__ldg(p.seq_lens + b), p.Smax);
+      nt = tiles_of(L);
+    } while (nt == 0);
+  }
+};
+
+// Index of the block whose tile range holds global tile x.
+__device__ __forceinline__ int block_of_tile(long long x, long long N, int P) {
+  return static_cast<int>(((x + 1) * P - 1) / N);
+}
+
+// 16-bit tile: D/64 boxes of [64 tokens][128 B], 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz16(int t, int chunk) {
+  const int box = chunk >> 3, c = chunk & 7;
+  return static_cast<uint32_t>(box * (kTileTokens * 128) + t * 128 +
+                               ((c ^ (t & 7)) << 4));
+}
+
+// E4M3 tile: [64 tokens][D bytes]; 128-byte swizzle at D=128, 64-byte at 64.
+template <int D>
+__device__ __forceinline__ uint32_t swz8(int t, int chunk) {
+  if constexpr (D == 128) {
+    return static_cast<uint32_t>(t * 128 + ((chunk ^ (t & 7)) << 4));
+  } else {
+    return static_cast<uint32_t>(t * 64 + ((chunk ^ ((t >> 1) & 3)) << 4));
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half x) {
+  return __half2float(x);
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <bool kBF16>
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
+  if constexpr (kBF16) {
+    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+  }
+}
+
+// Block-wide int64 sum over all kThreads threads (uses `red` scratch).
+__device__ __forceinline__ long long block_sum(long long v, long long* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  long long s = 0;
+  for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+  __syncthreads();
+  return s;
+}
+
+// Block-wide inclusive scan of int64 (uses `red` scratch).  Returns the
+// inclusive prefix; *total receives the block sum.
+__device__ __forceinline__ long long block_incl_scan(long long v,
+                                                     long long* red,
+                                                     long long* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  long long before = 0, all = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) before += red[w];
+    all += red[w];
+  }
+  __syncthreads();
+  *total = all;
+  return before + x;
+}
+
+template <int KV, bool QBF16, int D, int HB>
+__global__ void __launch_bounds__(kThreads, 1)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v,
+                      const DecodeParams p) {
+  using C = Cfg<KV, D, HB>;
+  constexpr bool kFp8 = (KV == kKvE4M3);
+  constexpr bool kMmaBF16 = !kFp8 && QBF16;
+  using QT = typename std::conditional<QBF16, __nv_bfloat16, __half>::type;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  float* mrg_o = reinterpret_cast<float*>(ring + C::kRingBytes);
+  float* mrg_m = mrg_o + kConsumerWarps * 16 * D;
+  float* mrg_l = mrg_m + kConsumerWarps * 16;
+  uint64_t* full = reinterpret_cast<uint64_t*>(mrg_l + kConsumerWarps * 16);
+  uint64_t* empty = full + C::kStages;
+  __shared__ long long s_red[kThreads / 32];
+  __shared__ long long s_pref0;
+  __shared__ int s_b0;
+  __shared__ int s_found;
+  __shared__ volatile int s_abort;
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int P = gridDim.x;
+  const int cta = blockIdx.x;
+  const int HU = p.Hkv * p.NHC;  // units per sequence
+
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], kConsumerWarps);
+    }
+    ptx::fence_barrier_init();
+    s_abort = 0;
+    s_found = 0;
+    s_b0 = 0;
+    s_pref0 = 0;
+  }
+
+  // ---- flat tile list: total N, this block's range, its first sequence ----
+  long long mine = 0;
+  for (int b = tid; b < p.B; b += kThreads)
+    mine += static_cast<long long>(
+                tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
+  const long long N = block_sum(mine, s_red);
+  const long long t0 = N * cta / P;
+  const long long t1 = N * (cta + 1) / P;
+  if (t0 < t1) {
+    long long run = 0;
+    for (int base = 0; base < p.B; base += kThreads) {
+      const int b = base + tid;
+      long long v = 0;
+      if (b < p.B)
+        v = static_cast<long long>(
+                tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
+      long long tot;
+      const long long incl = block_incl_scan(v, s_red, &tot);
+      const long long excl = incl - v;
+      if (v > 0 && run + excl <= t0 && t0 < run + incl) {
+        s_b0 = b;
+        s_pref0 = run + excl;
+        s_found = 1;
+      }
+      run += tot;
+      __syncthreads();
+      if (s_found) break;
+    }
+  }
+  __syncthreads();
+
+  TileWalk w0;
+  if (t0 < t1) {
+    w0.b = s_b0;
+    w0.L = clamp_len(__ldg(p.seq_lens + w0.b), p.Smax);
+    w0.nt = tiles_of(w0.L);
+    w0.pref = s_pref0;
+    const long long off = t0 - w0.pref;
+    w0.j = static_cast<int>(off / w0.nt);
+    w0.ti = static_cast<int>(off % w0.nt);
+  }
+
+  if (warp == kConsumerWarps) {
+    // =============================== producer ===============================
+    if (lane == 0 && t0 < t1) {
+      ptx::prefetch_tensormap(&map_k);
+      ptx::prefetch_tensormap(&map_v);
+      const uint64_t policy = ptx::policy_evict_first();
+      TileWalk w = w0;
+      long long it = 0;
+      for (long long g = t0; g < t1; ++g, ++it) {
+        const int stage = static_cast<int>(it % C::kStages);
+        const uint32_t ph = static_cast<uint32_t>((it / C::kStages) & 1);
+        if (!ptx::mbar_wait_bounded(&empty[stage], ph ^ 1u, kWaitLimitNs)) {
+          atomicOr(p.error, kErrWaitTimeout);
+          s_abort = 1;
+          break;
+        }
+        if (s_abort) break;
+        ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        const int plane = w.b * p.Hkv + w.j / p.NHC;
+        const int tok = w.ti * kTileTokens;
+        uint8_t* ks = ring + stage * C::kStageBytes;
+        uint8_t* vs = ks + C::kTileBytes;
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxesPerTile; ++bx) {
+          ptx::tma_load_3d(ks + bx * C::kBoxBytes, &map_k, &full[stage],
+                           bx * C::kBoxElems, tok, plane, policy);
+          ptx::tma_load_3d(vs + bx * C::kBoxBytes, &map_v, &full[stage],
+                           bx * C::kBoxElems, tok, plane, policy);
+        }
+        w.next(p, HU);
+      }
+      // Never leave the block with bulk copies still writing its memory.
+      const long long issued = it;
+      for (int s = 0; s < C::kStages; ++s) {
+        const long long uses =
+            issued > s ? (issued - s + C::kStages - 1) / C::kStages : 0;
+        if (uses > 0)
+          ptx::mbar_wait_bounded(&full[s],
+                                 static_cast<uint32_t>((uses - 1) & 1),
+                                 kDrainLimitNs);
+      }
+    }
+    return;
+  }
+
+  // ================================ consumers ===============================
+  const int cw = warp;                       // consumer warp 0..3
+  const int ct = tid;                        // consumer thread 0..127
+  const int hb = cw / C::kWarpsPerBlock;     // head block of this warp
+  const int wsl = cw % C::kWarpsPerBlock;    // token slice of this warp
+  const int r = lane >> 2, cq = lane & 3;    // mma fragment coordinates
+
+  // Sequences with no valid token: all-zero output rows.
+  for (int b = cta; b < p.B; b += P) {
+    if (clamp_len(__ldg(p.seq_lens + b), p.Smax) != 0) continue;
+    const size_t base = static_cast<size_t>(b) * p.Hq * D;
+    for (int i = ct; i < p.Hq * D; i += kConsumerWarps * 32)
+      store_out<QBF16>(p.out, base + i, 0.f);
+  }
+  if (t0 >= t1) return;
+
+  TileWalk w = w0;
+  uint32_t qf[C::kQSteps][4];
+  float o[C::kOTiles][4];
+  float m[2], l[2];
+  float s_mult = 0.f, o_mult = 1.f;
+  bool fresh = true;
+
+  long long it = 0;
+  for (long long g = t0; g < t1; ++g, ++it) {
+    const int kvh = w.j / p.NHC, hc = w.j % p.NHC;
+    if (fresh) {
+      // ---- new unit: query fragments, softmax state, multipliers ----
+      fresh = false;
+      const int row0 = hb * 16 + r, row1 = row0 + 8;
+      const bool ok0 = row0 < p.R && hc * p.R + row0 < p.G;
+      const bool ok1 = row1 < p.R && hc * p.R + row1 < p.G;
+      const int h0 = kvh * p.G + hc * p.R + row0;
+      const int h1 = h0 + 8;
+      const QT* q0 = reinterpret_cast<const QT*>(p.q) +
+                     (static_cast<size_t>(w.b) * p.Hq + (ok0 ? h0 : 0)) * D;
+      const QT* q1 = reinterpret_cast<const QT*>(p.q) +
+                     (static_cast<size_t>(w.b) * p.Hq + (ok1 ? h1 : 0)) * D;
+      if constexpr (!kFp8) {
+        // A fragment of k-step ks: (row r, d = 16ks + 2cq + {0,1}),
+        // (row r+8, same), (row r, +8), (row r+8, +8).
+#pragma unroll
+        for (int ks = 0; ks < C::kQSteps; ++ks) {
+          const int d0 = 16 * ks + 2 * cq;
+          qf[ks][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
+          qf[ks][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d0) : 0u;
+          qf[ks][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
+          qf[ks][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d0 + 8) : 0u;
+        }
+        s_mult = p.scale_log2;
+        o_mult = 1.f;
+      } else {
+        // The k index of the QK product is permuted so that each thread's K
+        // bytes are one contiguous run of its token row: thread column cq owns
+        // d in [cq*D/4, (cq+1)*D/4); k-step ks uses d = cq*D/4 + 4ks + {0..3}.
+        constexpr int kRun = D / 4;
+        float qa[kRun], qb[kRun];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRun; ++i) {
+          qa[i] = ok0 ? to_f32<QT>(q0[cq * kRun + i]) : 0.f;
+          qb[i] = ok1 ? to_f32<QT>(q1[cq * kRun + i]) : 0.f;
+          amax = fmaxf(amax, fmaxf(fabsf(qa[i]), fabsf(qb[i])));
+        }
+        for (int off = 16; off > 0; off >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        // Power of two putting the largest |q| in [2^14, 2^15): exact, and
+        // no q value can overflow f16.
+        int e = 0;
+        if (amax > 0.f) {
+          int ex;
+          frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
+          e = 15 - ex;
+          e = e > 100 ? 100 : (e < -100 ? -100 : e);
+        }
+        const float up = ldexpf(1.f, e);
+#pragma unroll
+        for (int ks = 0; ks < C::kQSteps; ++ks) {
+          qf[ks][0] = ptx::pack2<false>(qa[4 * ks] * up, qa[4 * ks + 1] * up);
+          qf[ks][1] = ptx::pack2<false>(qb[4 * ks] * up, qb[4 * ks + 1] * up);
+          qf[ks][2] = ptx::pack2<false>(qa[4 * ks + 2] * up,
+                                        qa[4 * ks + 3] * up);
+          qf[ks][3] = ptx::pack2<false>(qb[4 * ks + 2] * up,
+                                        qb[4 * ks + 3] * up);
+        }
+        const int sidx = w.b * p.Hkv + kvh;
+        s_mult = p.scale_log2 * __ldg(p.k_scale + sidx) * ldexpf(1.f, -e);
+        o_mult = __ldg(p.v_scale + sidx);
+      }
+#pragma unroll
+      for (int n = 0; n < C::kOTiles; ++n)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      m[0] = m[1] = -INFINITY;
+      l[0] = l[1] = 0.f;
+    }
+
+    // ---- wait for the stage ----
+    const int stage = static_cast<int>(it % C::kStages);
+    const uint32_t ph = static_cast<uint32_t>((it / C::kStages) & 1);
+    if (!s_abort && !ptx::mbar_wait_bounded(&full[stage], ph, kWaitLimitNs)) {
+      atomicOr(p.error, kErrWaitTimeout);
+      s_abort = 1;
+    }
+    const uint32_t kbase = ptx::smem_u32(ring + stage * C::kStageBytes);
+    const uint32_t vbase = kbase + C::kTileBytes;
+    const int L = w.L;
+    const int tok0 = w.ti * kTileTokens + wsl * C::kWarpTokens;  // in-seq
+    const int trow0 = wsl * C::kWarpTokens;                      // in-tile
+    const bool tail = (w.ti == w.nt - 1);
+
+    // ---- S = Q K^T for this warp's tokens ----
+    float s[C::kSTiles][4];
+#pragma unroll
+    for (int n = 0; n < C::kSTiles; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+
+    if constexpr (!kFp8) {
+      const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+      for (int ks = 0; ks < C::kQSteps; ++ks) {
+#pragma unroll
+        for (int np = 0; np < C::kSTiles / 2; ++np) {
+          const int t = trow0 + np * 16 + (mi >> 1) * 8 + rr;
+          const int chunk = 2 * ks + (mi & 1);
+          uint32_t b0, b1, b2, b3;
+          ptx::ldsm_x4(kbase + swz16(t, chunk), b0, b1, b2, b3);
+          ptx::mma16816<kMmaBF16>(s[2 * np], qf[ks], b0, b1);
+          ptx::mma16816<kMmaBF16>(s[2 * np + 1], qf[ks], b2, b3);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int n = 0; n < C::kSTiles; ++n) {
+        const int t = trow0 + n * 8 + r;
+        uint32_t kw[D / 16];
+        if constexpr (D == 128) {
+          const uint4 a = ptx::lds128(kbase + swz8<D>(t, 2 * cq));
+          const uint4 b = ptx::lds128(kbase + swz8<D>(t, 2 * cq + 1));
+          kw[0] = a.x; kw[1] = a.y; kw[2] = a.z; kw[3] = a.w;
+          kw[4] = b.x; kw[5] = b.y; kw[6] = b.z; kw[7] = b.w;
+        } else {
+          const uint4 a = ptx::lds128(kbase + swz8<D>(t, cq));
+          kw[0] = a.x; kw[1] = a.y; kw[2] = a.z; kw[3] = a.w;
+        }
+#pragma unroll
+        for (int ks = 0; ks < C::kQSteps; ++ks) {
+          const uint32_t b0 = ptx::e4m3x2_to_f16x2(kw[ks] & 0xffffu);
+          const uint32_t b1 = ptx::e4m3x2_to_f16x2(kw[ks] >> 16);
+          ptx::mma16816<false>(s[n], qf[ks], b0, b1);
+        }
+      }
+    }
+
+    // ---- online softmax (log2 domain) ----
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < C::kSTiles; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = s[n][e] * s_mult;
+        if (tail) {
+          const int tk = tok0 + n * 8 + 2 * cq + (e & 1);
+          if (tk >= L) v = -INFINITY;
+        }
+        s[n][e] = v;
+      }
+      mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+    const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float al0 = ptx::ex2(m[0] - base0), al1 = ptx::ex2(m[1] - base1);
+    m[0] = mn0;
+    m[1] = mn1;
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < C::kSTiles; ++n) {
+      s[n][0] = ptx::ex2(s[n][0] - base0);
+      s[n][1] = ptx::ex2(s[n][1] - base0);
+      s[n][2] = ptx::ex2(s[n][2] - base1);
+      s[n][3] = ptx::ex2(s[n][3] - base1);
+      rs0 += s[n][0] + s[n][1];
+      rs1 += s[n][2] + s[n][3];
+    }
+    l[0] = l[0] * al0 + rs0;
+    l[1] = l[1] * al1 + rs1;
+    if (al0 != 1.f || al1 != 1.f) {
+#pragma unroll
+      for (int n = 0; n < C::kOTiles; ++n) {
+        o[n][0] *= al0;
+        o[n][1] *= al0;
+        o[n][2] *= al1;
+        o[n][3] *= al1;
+      }
+    }
+
+    // ---- O += P V ----
+    constexpr bool kPBF16 = kMmaBF16;
+#pragma unroll
+    for (int kk = 0; kk < C::kPSteps; ++kk) {
+      uint32_t pa[4];
+      pa[0] = ptx::pack2<kPBF16>(s[2 * kk][0], s[2 * kk][1]);
+      pa[1] = ptx::pack2<kPBF16>(s[2 * kk][2], s[2 * kk][3]);
+      pa[2] = ptx::pack2<kPBF16>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[3] = ptx::pack2<kPBF16>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      // tokens (in sequence) of this thread's B-fragment k slots
+      const int tk = tok0 + kk * 16 + 2 * cq;
+      if constexpr (!kFp8) {
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (tail) {
+          mlo = (tk < L ? 0x0000ffffu : 0u) | (tk + 1 < L ? 0xffff0000u : 0u);
+          mhi = (tk + 8 < L ? 0x0000ffffu : 0u) |
+                (tk + 9 < L ? 0xffff0000u : 0u);
+        }
+        const int mi = lane >> 3, rr = lane & 7;
+        const int t = trow0 + kk * 16 + (mi & 1) * 8 + rr;
+#pragma unroll
+        for (int jp = 0; jp < C::kOTiles / 2; ++jp) {
+          uint32_t b0, b1, b2, b3;
+          ptx::ldsm_x4_trans(vbase + swz16(t, 2 * jp + (mi >> 1)), b0, b1, b2,
+                             b3);
+          b0 &= mlo;
+          b2 &= mlo;
+          b1 &= mhi;
+          b3 &= mhi;
+          ptx::mma16816<kMmaBF16>(o[2 * jp], pa, b0, b1);
+          ptx::mma16816<kMmaBF16>(o[2 * jp + 1], pa, b2, b3);
+        }
+      } else {
+        // Output columns are permuted too: thread row r owns d in
+        // [r*D/8, (r+1)*D/8); n-tile jn holds d = r*D/8 + jn.
+        const int ta = trow0 + kk * 16 + 2 * cq;
+        constexpr int kW = D / 32;  // 32-bit words per thread per token row
+        uint32_t xa[kW], xb[kW], xc[kW], xd[kW];
+        if constexpr (D == 128) {
+          const uint4 a = ptx::lds128(kbase + C::kTileBytes + swz8<D>(ta, r));
+          const uint4 b = ptx::lds128(kbase + C::kTileBytes + swz8<D>(ta + 1, r));
+          const uint4 c = ptx::lds128(kbase + C::kTileBytes + swz8<D>(ta + 8, r));
+          const uint4 d = ptx::lds128(kbase + C::kTileBytes + swz8<D>(ta + 9, r));
+          xa[0] = a.x; xa[1] = a.y; xa[2] = a.z; xa[3] = a.w;
+          xb[0] = b.x; xb[1] = b.y; xb[2] = b.z; xb[3] = b.w;
+          xc[0] = c.x; xc[1] = c.y; xc[2] = c.z; xc[3] = c.w;
+          xd[0] = d.x; xd[1] = d.y; xd[2] = d.z; xd[3] = d.w;
+        } else {
+          const int half = (r & 1) * 8;
+          const uint2 a = ptx::lds64(vbase + swz8<D>(ta, r >> 1) + half);
+          const uint2 b = ptx::lds64(vbase + swz8<D>(ta + 1, r >> 1) + half);
+          const uint2 c = ptx::lds64(vbase + swz8<D>(ta + 8, r >> 1) + half);
+          const uint2 d = ptx::lds64(vbase + swz8<D>(ta + 9, r >> 1) + half);
+          xa[0] = a.x; xa[1] = a.y;
+          xb[0] = b.x; xb[1] = b.y;
+          xc[0] = c.x; xc[1] = c.y;
+          xd[0] = d.x; xd[1] = d.y;
+        }
+        if (tail) {
+          const uint32_t ka = tk < L ? ~0u : 0u, kb = tk + 1 < L ? ~0u : 0u;
+          const uint32_t kc = tk + 8 < L ? ~0u : 0u, kd = tk + 9 < L ? ~0u : 0u;
+#pragma unroll
+          for (int i = 0; i < kW; ++i) {
+            xa[i] &= ka;
+            xb[i] &= kb;
+            xc[i] &= kc;
+            xd[i] &= kd;
+          }
+        }
+#pragma unroll
+        for (int wi = 0; wi < kW; ++wi) {
+          const uint32_t p01 = __byte_perm(xa[wi], xb[wi], 0x5140);
+          const uint32_t p23 = __byte_perm(xa[wi], xb[wi], 0x7362);
+          const uint32_t q01 = __byte_perm(xc[wi], xd[wi], 0x5140);
+          const uint32_t q23 = __byte_perm(xc[wi], xd[wi], 0x7362);
+          ptx::mma16816<false>(o[4 * wi + 0], pa,
+                               ptx::e4m3x2_to_f16x2(p01 & 0xffffu),
+                               ptx::e4m3x2_to_f16x2(q01 & 0xffffu));
+          ptx::mma16816<false>(o[4 * wi + 1], pa,
+                               ptx::e4m3x2_to_f16x2(p01 >> 16),
+                               ptx::e4m3x2_to_f16x2(q01 >> 16));
+          ptx::mma16816<false>(o[4 * wi + 2], pa,
+                               ptx::e4m3x2_to_f16x2(p23 & 0xffffu),
+                               ptx::e4m3x2_to_f16x2(q23 & 0xffffu));
+          ptx::mma16816<false>(o[4 * wi + 3], pa,
+                               ptx::e4m3x2_to_f16x2(p23 >> 16),
+                               ptx::e4m3x2_to_f16x2(q23 >> 16));
+        }
+      }
+    }
+
+    // ---- release the stage ----
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&empty[stage]);
+
+    const bool unit_end = (w.ti == w.nt - 1) || (g == t1 - 1);
+    if (unit_end) {
+      // ================= unit (segment) epilogue =================
+      const int u = w.b * HU + w.j;
+      const long long us = w.pref + static_cast<long long>(w.j) * w.nt;
+      const int c_first = block_of_tile(us, N, P);
+      const int c_last = block_of_tile(us + w.nt - 1, N, P);
+      const bool whole = (c_first == c_last);
+
+      // 1) this warp's state -> shared memory, canonical [row][d] layout
+      float lt0 = l[0], lt1 = l[1];
+      lt0 += __shfl_xor_sync(0xffffffffu, lt0, 1);
+      lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+      lt1 += __shfl_xor_sync(0xffffffffu, lt1, 1);
+      lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+      float* mo = mrg_o + cw * 16 * D;
+#pragma unroll
+      for (int n = 0; n < C::kOTiles; ++n) {
+        int d0, d1;
+        if constexpr (!kFp8) {
+          d0 = 8 * n + 2 * cq;
+          d1 = d0 + 1;
+        } else {
+          d0 = (2 * cq) * (D / 8) + n;
+          d1 = (2 * cq + 1) * (D / 8) + n;
+        }
+        mo[r * D + d0] = o[n][0];
+        mo[r * D + d1] = o[n][1];
+        mo[(r + 8) * D + d0] = o[n][2];
+        mo[(r + 8) * D + d1] = o[n][3];
+      }
+      if (cq == 0) {
+        mrg_m[cw * 16 + r] = m[0];
+        mrg_m[cw * 16 + r + 8] = m[1];
+        mrg_l[cw * 16 + r] = lt0;
+        mrg_l[cw * 16 + r + 8] = lt1;
+      }
+      ptx::named_bar_sync(1, kConsumerWarps * 32);
+
+      // 2) merge the warps of each head block; write out or write a partial
+      const int slot = c_first == c_last ? 0 : cta + u;
+      for (int idx = ct; idx < C::kRowsPad * D; idx += kConsumerWarps * 32) {
+        const int row = idx / D, d = idx % D;
+        if (row >= p.R || hc * p.R + row >= p.G) continue;
+        const int hbk = row >> 4, rr = row & 15;
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < C::kWarpsPerBlock; ++k)
+          M = fmaxf(M, mrg_m[(hbk * C::kWarpsPerBlock + k) * 16 + rr]);
+        const float Mb = (M == -INFINITY) ? 0.f : M;
+        float lt = 0.f, acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < C::kWarpsPerBlock; ++k) {
+          const int wk = hbk * C::kWarpsPerBlock + k;
+          const float f = ptx::ex2(mrg_m[wk * 16 + rr] - Mb);
+          lt += mrg_l[wk * 16 + rr] * f;
+          acc += mrg_o[(wk * 16 + rr) * D + d] * f;
+        }
+        const float val = lt > 0.f ? acc / lt : 0.f;
+        if (whole) {
+          const int h = kvh * p.G + hc * p.R + row;
+          store_out<QBF16>(p.out,
+                           (static_cast<size_t>(w.b) * p.Hq + h) * D + d,
+                           val * o_mult);
+        } else {
+          const size_t prow = static_cast<size_t>(slot) * C::kRowsPad + row;
+          p.part_o[prow * D + d] = val;
+          if (d == 0) p.part_lse[prow] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
+        }
+      }
+
+      if (!whole) {
+        // 3) count arrivals; the last block of the unit combines the partials
+        __threadfence();
+        ptx::named_bar_sync(1, kConsumerWarps * 32);
+        if (ct == 0) {
+          const uint32_t n_cover = static_cast<uint32_t>(c_last - c_first + 1);
+          const uint32_t ticket = atomicAdd(p.counters + u, 1u);
+          s_last = (ticket == n_cover - 1) ? 1 : 0;
+        }
+        ptx::named_bar_sync(1, kConsumerWarps * 32);
+        if (s_last) {
+          __threadfence();
+          for (int idx = ct; idx < C::kRowsPad * D;
+               idx += kConsumerWarps * 32) {
+            const int row = idx / D, d = idx % D;
+            if (row >= p.R || hc * p.R + row >= p.G) continue;
+            float M = -INFINITY;
+            for (int c = c_first; c <= c_last; ++c)
+              M = fmaxf(M, __ldcg(p.part_lse +
+                                  static_cast<size_t>(c + u) * C::kRowsPad + row));
+            const float Mb = (M == -INFINITY) ? 0.f : M;
+            float lt = 0.f, acc = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const size_t prow = static_cast<size_t>(c + u) * C::kRowsPad + row;
+              const float f = ptx::ex2(__ldcg(p.part_lse + prow) - Mb);
+              lt += f;
+              acc += f * __ldcg(p.part_o + prow * D + d);
+            }
+            const int h = kvh * p.G + hc * p.R + row;
+            store_out<QBF16>(p.out,
+                             (static_cast<size_t>(w.b) * p.Hq + h) * D + d,
+                             (lt > 0.f ? acc / lt : 0.f) * o_mult);
+          }
+          if (ct == 0) p.counters[u] = 0u;
+        }
+      }
+      ptx::named_bar_sync(1, kConsumerWarps * 32);
+      fresh = true;
+    }
+    w.next(p, HU);
+  }
+}
+
+}  // namespace gqa

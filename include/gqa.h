@@ -1,0 +1,157 @@
+/*
+ * gqa.h — C ABI of the B300 (sm_103a) grouped-query attention decode library
+ * (libgqa_b300.so).
+ *
+ * The operation.  One decode step of grouped-query attention: Hq query heads
+ * share Hkv key/value heads; query head h reads KV head floor(h / G) with
+ * G = Hq / Hkv, so heads 0..G-1 share KV head 0, heads G..2G-1 share KV head 1,
+ * and so on ("Llama-2 70B uses 64 query heads, how many KV heads does it
+ * actually keep?", What the choice does to attention; "GQA, decode the
+ * acronym and describe its KV sharing pattern").  For every sequence b and
+ * query head h the new token's query attends over the L_b = seq_lens[b] cached
+ * tokens of its KV head with ordinary scaled dot-product attention:
+ *
+ *     s_t   = scale * dot(q[b,h,:], K[b,kvh,t,:])        t < L_b
+ *     w     = softmax(s)
+ *     out[b,h,:] = sum_t w_t * V[b,kvh,t,:]
+ *
+ * ("Grouped Query Attention (GQA): Efficient Multi-Head Attention", Worked
+ * example 2: score = q.k / sqrt(head_dim), softmax, weighted sum of values; the
+ * decode step attends over the cached K/V of all prior tokens, The
+ * bottleneck).  G = 1 is multi-head attention and Hkv = 1 is multi-query
+ * attention (same page, Two extremes).  The cache is read once per KV head and
+ * serves all G query heads of its group; it is never expanded to Hq heads
+ * ("Grouped Query Attention: Why 8 KV Heads Decide Your Batch Size", Why does
+ * GQA speed up decode, and the repeat_kv trap).
+ *
+ * Layout (all row-major, contiguous, in DEVICE memory owned by the caller):
+ *     q, out      [B, Hq, D]
+ *     k/v cache   [B, Hkv, Smax, D]   valid prefix t < seq_lens[b]
+ *     seq_lens    [B] int32
+ *     k/v scales  [B, Hkv] fp32        (FP8 cache only)
+ * Positions t >= seq_lens[b] are never used (they may hold anything, NaN
+ * included).  seq_lens values are read on the device and never copied to the
+ * host; a value below 0 counts as 0 and a value above Smax as Smax.  A
+ * sequence with no valid token produces an all-zero output row.  The caller
+ * appends the current token to the cache before the call.
+ *
+ * Numerics.  Products and sums are accumulated in fp32; the output is rounded
+ * to nearest-even into the q/out dtype.  Results do not depend on run order
+ * (no floating-point atomics): the same inputs on the same device give
+ * bit-identical outputs.
+ *
+ * Execution.  Every compute call is asynchronous on `stream` (a cudaStream_t;
+ * NULL means the legacy default stream) and never synchronises with the host.
+ * The library keeps a small scratch buffer per (device, stream) for the
+ * split-sequence partial results; it is allocated on the first call that needs
+ * it (stream-ordered, from the device's default memory pool) and kept for
+ * later calls.  Calls on one stream may follow each other freely; calls that
+ * share a stream must not run concurrently from several host threads.
+ *
+ * Errors.  Argument checks run on the host before anything is launched and
+ * return GQA_ERR_INVALID_ARG or GQA_ERR_UNSUPPORTED without touching the GPU.
+ * A CUDA error from a launch or an allocation returns GQA_ERR_CUDA.  No C++
+ * exception crosses this interface.  The library keeps no pointer to caller
+ * memory after a call returns.
+ */
+#ifndef GQA_B300_GQA_H_
+#define GQA_B300_GQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad scale  */
+  GQA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement   */
+  GQA_ERR_CUDA = 3,        /* a CUDA call failed (launch, allocation, ...)  */
+  GQA_ERR_DEVICE = 4       /* a kernel reported a fault: see gqa_device_errors */
+} gqa_status;
+
+typedef enum {
+  GQA_F16 = 0,  /* IEEE binary16                                  */
+  GQA_BF16 = 1, /* bfloat16                                       */
+  GQA_E4M3 = 2  /* OCP FP8 E4M3 ("e4m3fn"), cache elements only   */
+} gqa_dtype;
+
+/*
+ * gqa_decode — one GQA decode step with a 16-bit cache.
+ *
+ *   q        [B, Hq, D]        dtype, device, 16-byte aligned
+ *   k_cache  [B, Hkv, Smax, D] dtype, device, 16-byte aligned
+ *   v_cache  [B, Hkv, Smax, D] dtype, device, 16-byte aligned
+ *   seq_lens [B] int32, device, 4-byte aligned
+ *   scale    softmax scale, finite and > 0 (1/sqrt(D) by convention)
+ *   out      [B, Hq, D]        dtype, device, 16-byte aligned; fully written
+ *   B >= 1, Hkv >= 1, Hq % Hkv == 0, Smax >= 1, D in {64, 128}
+ *   dtype    GQA_F16 or GQA_BF16 (q, caches and out share it)
+ *
+ * Returns GQA_OK once the work is enqueued on `stream`.
+ */
+gqa_status gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* seq_lens, float scale, void* out, int B,
+                      int Hq, int Hkv, int Smax, int D, gqa_dtype dtype,
+                      void* stream);
+
+/*
+ * gqa_decode_fp8 — the same step with an FP8 E4M3 cache and one fp32 scale
+ * per (sequence, KV head) for K and one for V ("Grouped-Query Attention: How
+ * Sharing KV Heads Shrinks Inference Memory", FP8 KV cache: an 8-bit cache
+ * with scaling factors, halving the bytes read per step).  The cached value
+ * of element x of K[b, j] is e4m3(x) * k_scale[b*Hkv + j] (likewise for V).
+ *
+ *   k_cache, v_cache [B, Hkv, Smax, D] E4M3 bytes, device, 16-byte aligned
+ *   k_scale, v_scale [B, Hkv] fp32, device, 4-byte aligned, finite
+ *   qo_dtype         GQA_F16 or GQA_BF16: the dtype of q and out
+ * Other arguments as for gqa_decode.
+ */
+gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
+                          const void* v_cache, const float* k_scale,
+                          const float* v_scale, const int32_t* seq_lens,
+                          float scale, void* out, int B, int Hq, int Hkv,
+                          int Smax, int D, gqa_dtype qo_dtype, void* stream);
+
+/*
+ * gqa_kv_bytes_per_token — KV-cache bytes one token occupies across a model:
+ * 2 (K and V) x layers x kv_heads x head_dim x bytes_per_elem ("Grouped Query
+ * Attention: Why 8 KV Heads Decide Your Batch Size", TL;DR; e.g. 327,680 B =
+ * 320 KiB for 80 layers, 8 KV heads, head_dim 128, fp16).  Returns 0 if an
+ * argument is not positive.  Host only.
+ */
+size_t gqa_kv_bytes_per_token(int layers, int kv_heads, int head_dim,
+                              int bytes_per_elem);
+
+/* gqa_status_string — static, NUL-terminated description of a status. */
+const char* gqa_status_string(gqa_status status);
+
+/*
+ * gqa_device_errors — synchronises `stream`, then returns (and clears) the
+ * fault flags the kernels raised on it since the last query: 0 when none.
+ * Bit 0: a pipeline wait gave up after its time limit (the affected outputs
+ * are unspecified).  Returns GQA_ERR_CUDA if the synchronisation fails.
+ */
+gqa_status gqa_device_errors(void* stream, uint32_t* flags);
+
+/*
+ * gqa_set_num_ctas — test and tuning hook: fixes the number of persistent
+ * thread blocks the decode kernels launch (0 restores the default, one full
+ * wave of the device).  It changes how the sequence axis is split between
+ * blocks, never the result beyond fp32 rounding.  Process-wide; host only.
+ */
+void gqa_set_num_ctas(int num_ctas);
+
+/*
+ * gqa_last_launch_count — number of kernels the most recent compute call made
+ * from this host thread enqueued (0 if it returned before launching).
+ */
+int gqa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_B300_GQA_H_ */

@@ -1,0 +1,116 @@
+"""Host-only checks of the C-ABI library: it loads without a GPU, exports every
+function include/gqa.h declares, and rejects bad arguments on the host before
+any CUDA call (so these run on a machine with no GPU)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import grouped_query_attention_11_b300 as gq
+from grouped_query_attention_11_b300 import build as gq_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    gq_build.build()
+    return gq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert {"gqa_decode", "gqa_decode_fp8", "gqa_kv_bytes_per_token",
+            "gqa_status_string"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in gq.SIGNATURES, name
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((80, 8, 128, 2), 327_680), ((80, 64, 128, 2), 2_621_440),
+    ((80, 1, 128, 2), 40_960), ((32, 32, 128, 2), 524_288),
+    ((32, 8, 128, 2), 131_072), ((32, 1, 128, 2), 16_384),
+    ((32, 8, 128, 1), 65_536), ((40, 40, 128, 2), 819_200),
+    ((40, 8, 128, 2), 163_840), ((0, 8, 128, 2), 0), ((80, -1, 128, 2), 0),
+])
+def test_kv_bytes_per_token(L, args, expected):
+    # the pages' cache-size figures (cache-size formula, 2 x layers x kv_heads
+    # x head_dim x bytes per element)
+    assert gq.gqa_kv_bytes_per_token(*args) == expected
+
+
+def test_status_strings(L):
+    for st in range(5):
+        assert gq.gqa_status_string(st)
+    assert gq.gqa_status_string(99) == "unknown status"
+
+
+# Fake, well-aligned "device" addresses: the library must reject the call on
+# the host before it ever dereferences or hands them to CUDA.
+A = 1 << 20
+
+
+def _call(q=A, k=A * 2, v=A * 3, lens=A * 4, scale=0.125, out=A * 5, B=2,
+          Hq=8, Hkv=2, Smax=128, D=64, dtype=gq.GQA_BF16):
+    return gq.lib().gqa_decode(q, k, v, lens, scale, out, B, Hq, Hkv, Smax, D,
+                               dtype, None)
+
+
+def _call8(q=A, k=A * 2, v=A * 3, ks=A * 6, vs=A * 7, lens=A * 4, scale=0.125,
+           out=A * 5, B=2, Hq=8, Hkv=2, Smax=128, D=64, dtype=gq.GQA_BF16):
+    return gq.lib().gqa_decode_fp8(q, k, v, ks, vs, lens, scale, out, B, Hq,
+                                   Hkv, Smax, D, dtype, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(k=None), dict(v=None), dict(lens=None), dict(out=None),
+    dict(q=A + 8), dict(k=A * 2 + 2), dict(out=A * 5 + 4), dict(lens=A * 4 + 2),
+    dict(B=0), dict(B=-1), dict(Hq=0), dict(Hkv=0), dict(Hq=8, Hkv=3),
+    dict(Smax=0), dict(scale=0.0), dict(scale=-1.0), dict(scale=math.inf),
+    dict(scale=math.nan), dict(dtype=gq.GQA_E4M3), dict(dtype=7),
+])
+def test_decode_rejects_invalid_arguments(L, kw):
+    gq.lib().gqa_set_num_ctas(0)
+    assert _call(**kw) == gq.GQA_ERR_INVALID_ARG
+    assert gq.gqa_last_launch_count() == 0
+
+
+@pytest.mark.parametrize("kw", [dict(D=96), dict(D=256), dict(D=32)])
+def test_decode_unsupported_head_dim(L, kw):
+    assert _call(**kw) == gq.GQA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw", [
+    dict(ks=None), dict(vs=None), dict(ks=A * 6 + 2), dict(q=None),
+    dict(dtype=gq.GQA_E4M3), dict(Hq=6, Hkv=4), dict(scale=0.0),
+])
+def test_decode_fp8_rejects_invalid_arguments(L, kw):
+    assert _call8(**kw) == gq.GQA_ERR_INVALID_ARG
+
+
+def test_device_errors_rejects_null_flags(L):
+    assert gq.lib().gqa_device_errors(None, None) == gq.GQA_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_oracle_dependency():
+    # The CUDA library and its binding never import or link the oracle.
+    pkg = os.path.join(ROOT, "grouped_query_attention_11_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text
+                assert "liboracle" not in text and "gqa_oracle" not in text
