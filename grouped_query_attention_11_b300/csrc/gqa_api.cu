@@ -104,10 +104,19 @@ struct DeviceInfo {
 };
 std::map<int, DeviceInfo> g_dev;
 
-// Scratch per (device, stream): [error flags | counters | lse | partial O].
+// Scratch per (device, stream), in two allocations:
+//  * ctl  = [error flags (kHeaderBytes) | arrival counters, one per unit].
+//    Zeroed once when allocated; the kernels leave every counter at zero when
+//    they finish, so the region holds zeros between calls and is never
+//    re-initialised.  It is never shared with the partials: a counter must not
+//    land on bytes a previous call used for partial results.
+//  * part = [partial log2-sum-exp | partial O], fully written before it is
+//    read within one call; no initial value needed.
 struct Scratch {
-  void* ptr = nullptr;
-  size_t bytes = 0;
+  void* ctl = nullptr;
+  size_t ctl_units = 0;  // counter capacity
+  void* part = nullptr;
+  size_t part_bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 
@@ -142,29 +151,45 @@ cudaError_t configure(int dev, const Variant& v, int* sms, int* per_sm) {
   return cudaSuccess;
 }
 
-cudaError_t scratch_for(int dev, cudaStream_t stream, size_t need,
-                        void** out) {
+// Grows the stream's scratch to hold `units` counters and `part_need` bytes of
+// partials.  Allocation is stream-ordered (the device's default pool).
+cudaError_t scratch_for(int dev, cudaStream_t stream, size_t units,
+                        size_t part_need, Scratch** out) {
   Scratch& s = g_scratch[{dev, stream}];
-  if (s.bytes < need) {
-    if (s.ptr) {
-      cudaError_t e = cudaFreeAsync(s.ptr, stream);
-      s.ptr = nullptr;
-      s.bytes = 0;
+  if (s.ctl_units < units || !s.ctl) {
+    const size_t cap = align_up(units + units / 4 + 1024, 1024);
+    void* ctl = nullptr;
+    cudaError_t e = cudaMallocAsync(&ctl, kHeaderBytes + cap * 4, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(ctl, 0, kHeaderBytes + cap * 4, stream);
+    if (e != cudaSuccess) return e;
+    if (s.ctl) {
+      // carry the error flags over; the old counters are all zero
+      e = cudaMemcpyAsync(ctl, s.ctl, sizeof(uint32_t),
+                          cudaMemcpyDeviceToDevice, stream);
+      if (e != cudaSuccess) return e;
+      e = cudaFreeAsync(s.ctl, stream);
       if (e != cudaSuccess) return e;
     }
-    const size_t bytes = align_up(need + need / 4, 1 << 20);
-    cudaError_t e = cudaMallocAsync(&s.ptr, bytes, stream);
+    s.ctl = ctl;
+    s.ctl_units = cap;
+  }
+  if (s.part_bytes < part_need || !s.part) {
+    if (s.part) {
+      cudaError_t e = cudaFreeAsync(s.part, stream);
+      s.part = nullptr;
+      s.part_bytes = 0;
+      if (e != cudaSuccess) return e;
+    }
+    const size_t bytes = align_up(part_need + part_need / 4 + 1, 1 << 20);
+    cudaError_t e = cudaMallocAsync(&s.part, bytes, stream);
     if (e != cudaSuccess) {
-      s.ptr = nullptr;
+      s.part = nullptr;
       return e;
     }
-    // error flags and counters start (and stay, between calls) at zero;
-    // partials need no initial value.
-    e = cudaMemsetAsync(s.ptr, 0, bytes, stream);
-    if (e != cudaSuccess) return e;
-    s.bytes = bytes;
+    s.part_bytes = bytes;
   }
-  *out = s.ptr;
+  *out = &s;
   return cudaSuccess;
 }
 
@@ -217,18 +242,24 @@ gqa_status launch(const void* q, const void* k, const void* v,
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   int sms = 0, per_sm = 0;
   if (configure(dev, var, &sms, &per_sm) != cudaSuccess) return GQA_ERR_CUDA;
-  const int grid =
-      g_num_ctas_override > 0 ? g_num_ctas_override : sms * per_sm;
+  // Default: one full wave, but never more blocks than the largest possible
+  // number of tiles (seq_lens stay on the device; Smax bounds them).
+  const long long max_tiles =
+      units * ((static_cast<long long>(Smax) + kTileTokens - 1) / kTileTokens);
+  const long long wave = static_cast<long long>(sms) * per_sm;
+  const int grid = g_num_ctas_override > 0
+                       ? g_num_ctas_override
+                       : static_cast<int>(max_tiles < wave ? max_tiles : wave);
 
   const size_t slots = static_cast<size_t>(grid) + static_cast<size_t>(units);
-  const size_t cnt_bytes = align_up(static_cast<size_t>(units) * 4, 256);
   const size_t lse_bytes = align_up(slots * rows_pad * 4, 256);
   const size_t o_bytes = slots * rows_pad * static_cast<size_t>(D) * 4;
-  void* ws = nullptr;
-  if (scratch_for(dev, stream, kHeaderBytes + cnt_bytes + lse_bytes + o_bytes,
-                  &ws) != cudaSuccess)
+  Scratch* sc = nullptr;
+  if (scratch_for(dev, stream, static_cast<size_t>(units), lse_bytes + o_bytes,
+                  &sc) != cudaSuccess)
     return GQA_ERR_CUDA;
-  uint8_t* wb = static_cast<uint8_t*>(ws);
+  uint8_t* ctl = static_cast<uint8_t*>(sc->ctl);
+  uint8_t* part = static_cast<uint8_t*>(sc->part);
 
   DecodeParams p;
   p.q = q;
@@ -236,11 +267,10 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.seq_lens = seq_lens;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  p.error = reinterpret_cast<uint32_t*>(wb);
-  p.counters = reinterpret_cast<uint32_t*>(wb + kHeaderBytes);
-  p.part_lse = reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes);
-  p.part_o =
-      reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes + lse_bytes);
+  p.error = reinterpret_cast<uint32_t*>(ctl);
+  p.counters = reinterpret_cast<uint32_t*>(ctl + kHeaderBytes);
+  p.part_lse = reinterpret_cast<float*>(part);
+  p.part_o = reinterpret_cast<float*>(part + lse_bytes);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.B = B;
   p.Hq = Hq;
@@ -331,11 +361,11 @@ gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   auto it = gqa::g_scratch.find({dev, stream});
-  if (it == gqa::g_scratch.end() || !it->second.ptr) return GQA_OK;
+  if (it == gqa::g_scratch.end() || !it->second.ctl) return GQA_OK;
   uint32_t v = 0;
-  if (cudaMemcpy(&v, it->second.ptr, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(&v, it->second.ctl, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
     return GQA_ERR_CUDA;
-  if (v != 0 && cudaMemset(it->second.ptr, 0, 4) != cudaSuccess)
+  if (v != 0 && cudaMemset(it->second.ctl, 0, 4) != cudaSuccess)
     return GQA_ERR_CUDA;
   *flags = v;
   return GQA_OK;

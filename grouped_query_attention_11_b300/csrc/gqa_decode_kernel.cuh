@@ -251,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int P = gridDim.x;
   const int cta = blockIdx.x;
   const int HU = p.Hkv * p.NHC;  // units per sequence
 
@@ -273,8 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mine += static_cast<long long>(
                 tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
   const long long N = block_sum(mine, s_red);
-  const long long t0 = N * cta / P;
-  const long long t1 = N * (cta + 1) / P;
+  // Blocks that take part: at most one per tile, so that every block in a
+  // unit's covering range [c_first, c_last] owns at least one of its tiles
+  // (the arrival count of the split combine relies on it).
+  const int P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
+  const long long t0 = cta < P ? N * cta / P : 0;
+  const long long t1 = cta < P ? N * (cta + 1) / P : 0;
   if (t0 < t1) {
     long long run = 0;
     for (int base = 0; base < p.B; base += kThreads) {
@@ -362,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = lane >> 2, cq = lane & 3;    // mma fragment coordinates
 
   // Sequences with no valid token: all-zero output rows.
-  for (int b = cta; b < p.B; b += P) {
+  for (int b = cta; b < p.B; b += gridDim.x) {
     if (clamp_len(__ldg(p.seq_lens + b), p.Smax) != 0) continue;
     const size_t base = static_cast<size_t>(b) * p.Hq * D;
     for (int i = ct; i < p.Hq * D; i += kConsumerWarps * 32)

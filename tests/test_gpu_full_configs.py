@@ -18,6 +18,7 @@ def sample_rows(w, seq_lens, n_target=96, seed=0):
     """(b, h) pairs: first/last sequence, shortest/longest sequence, every
     KV-group boundary head of those, plus a seeded random spread."""
     rng = np.random.default_rng(seed)
+    n_target = min(n_target, w.B * w.Hq)
     lens = seq_lens.numpy()
     bs = {0, w.B - 1, int(lens.argmin()), int(lens.argmax())}
     pairs = set()

@@ -271,3 +271,23 @@ def test_output_written_in_place_and_stream_respected():
     s.synchronize()
     assert torch.isfinite(out).all()
     assert gq.gqa_device_errors(s) == 0
+
+
+def test_scratch_reuse_across_unit_counts(oracle_mod):
+    """Calls on one stream whose unit counts go up and down: the split-combine
+    counters of a call with many units must not pick up the partial results a
+    call with few units left behind in the library's scratch."""
+    shapes = [
+        # B, Hq, Hkv, D, Smax, lens  (units = B * Hkv)
+        (2, 64, 1, 128, 900, ("list", 900, 700)),       # 2 units, many splits
+        (3, 64, 64, 128, 700, ("uniform",)),            # 192 units
+        (1, 32, 2, 128, 1000, ("uniform",)),            # 2 units
+        (4, 16, 16, 64, 500, ("list", 500, 3, 250, 499)),  # 64 units
+        (3, 64, 64, 128, 700, ("uniform",)),
+    ]
+    for i, (B, Hq, Hkv, D, Smax, lens) in enumerate(shapes):
+        w = Workload(f"reuse{i}", B, Hq, Hkv, D, Smax, "bf16", lens=lens,
+                     seed=60 + i)
+        inp = make_inputs(w, pad="nan")
+        out = run_cuda(inp)
+        assert_contract(out, oracle_full(oracle_mod, inp), w.name)
