@@ -185,6 +185,52 @@ def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens,
     return out
 
 
+class BoundDecode:
+    """One decode call with its arguments checked and marshalled once.
+
+    ``BoundDecode(inp, out, stream)()`` enqueues the same gqa_decode /
+    gqa_decode_fp8 call as :func:`decode_inputs` would, but each call is a
+    single C-ABI call with pre-built arguments: for loops that launch the
+    same step many times (benchmarks, graph-free decode loops), the host cost
+    per step is then only the library's own.  The tensors must stay alive and
+    in place while the object is used.
+    """
+
+    def __init__(self, inp: dict, out, stream=None):
+        fp8 = inp.get("k_scale") is not None
+        # run the full checks once, through the public entry points
+        if fp8:
+            gqa_decode_fp8(inp["q"], inp["k"], inp["v"], inp["k_scale"],
+                           inp["v_scale"], inp["seq_lens"], inp["scale"],
+                           out=out, stream=stream)
+        else:
+            gqa_decode(inp["q"], inp["k"], inp["v"], inp["seq_lens"],
+                       inp["scale"], out=out, stream=stream)
+        q, k = inp["q"], inp["k"]
+        B, Hq, D = q.shape
+        _, Hkv, Smax, _ = k.shape
+        h = _stream_handle(stream)
+        if fp8:
+            self._fn = lib().gqa_decode_fp8
+            self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),
+                          inp["k_scale"].data_ptr(), inp["v_scale"].data_ptr(),
+                          inp["seq_lens"].data_ptr(), float(inp["scale"]),
+                          out.data_ptr(), B, Hq, Hkv, Smax, D, _dtype_code(q),
+                          h)
+        else:
+            self._fn = lib().gqa_decode
+            self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),
+                          inp["seq_lens"].data_ptr(), float(inp["scale"]),
+                          out.data_ptr(), B, Hq, Hkv, Smax, D, _dtype_code(q),
+                          h)
+        self._keep = (inp, out)
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != GQA_OK:
+            raise GQAError(st, self._fn.__name__)
+
+
 def decode_inputs(inp: dict, out=None, stream=None):
     """Runs the right entry point on a dict of CUDA tensors (the layout the
     input generator produces, moved to the device)."""

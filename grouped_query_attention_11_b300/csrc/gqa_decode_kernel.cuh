@@ -21,11 +21,15 @@
 //    swizzle, L2 evict-first) of the K and V tiles into a multi-stage shared
 //    memory ring guarded by mbarriers.  Each KV byte is read from HBM once and
 //    serves all query heads of its group from shared memory.
-//  * Group-batched math.  Four consumer warps hold the group's query rows as
-//    mma A fragments (16 rows per head block; G < 16 pads with zero rows) and
-//    run QK^T and PV through mma.sync m16n8k16 with fp32 accumulation.  The
-//    online softmax (running row max, rescale, row sum) lives in registers;
-//    row reductions are two quad shuffles.
+//  * Group-batched math.  Consumer warps hold the group's query rows as mma
+//    A fragments (16 rows per head block; G < 16 pads with zero rows) and run
+//    QK^T and PV through mma.sync m16n8k16 with fp32 accumulation.  The online
+//    softmax (running row max, rescale, row sum) lives in registers; row
+//    reductions are two quad shuffles.
+//  * Ping-pong consumers.  Two groups of four consumer warps take alternate
+//    ring stages, each with its own softmax state, so that one group's
+//    dependent mma / exp chains overlap the other's; the states of both groups
+//    merge at the end of every unit.
 //  * FP8 E4M3 cache.  Bytes are turned into exact f16 pairs in registers
 //    (cvt.rn.f16x2.e4m3x2); q is moved into f16 with a per-head-block power
 //    of two so no value can overflow; k_scale and the power of two fold into
@@ -53,12 +57,15 @@
 namespace gqa {
 
 constexpr int kTileTokens = 64;   // tokens per pipeline stage
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kGroupWarps = 4;     // consumer warps per ping-pong group
+constexpr int kGroups = 2;         // groups taking alternate ring stages
+constexpr int kConsumerWarps = kGroups * kGroupWarps;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kMaxUnitRows = 64;  // query heads per unit (4 head blocks)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 220 * 1024;
 
 enum KvKind : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
 
@@ -93,7 +100,7 @@ struct Cfg {
   static constexpr int kBoxElems = (KV == kKvE4M3) ? D : 64;
   static constexpr int kBoxBytes = kTileTokens * kBoxElems * kElemBytes;
   static constexpr int kBoxesPerTile = D / kBoxElems;
-  static constexpr int kWarpsPerBlock = kConsumerWarps / HB;  // per head block
+  static constexpr int kWarpsPerBlock = kGroupWarps / HB;  // per head block
   static constexpr int kWarpTokens = kTileTokens / kWarpsPerBlock;
   static constexpr int kSTiles = kWarpTokens / 8;   // S n-tiles per warp
   static constexpr int kPSteps = kWarpTokens / 16;  // PV k-steps per warp
@@ -102,14 +109,22 @@ struct Cfg {
   static constexpr int kRowsPad = HB * 16;
   static constexpr int kMergeBytes =
       kConsumerWarps * 16 * D * 4 + 2 * kConsumerWarps * 16 * 4;
-  static constexpr int kStagesRaw = (kSmemBudget - kMergeBytes - 1024) /
+  static constexpr int kStagesRaw = (kSmemBudget - kMergeBytes - 1024 - 256) /
                                     kStageBytes;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  // Even, so that stage s is always consumed by ping-pong group s % 2: each
+  // group then waits on the phases of its stages strictly in order, which the
+  // mbarrier parity test requires.
+  static constexpr int kStages = (kStagesRaw > 16 ? 16 : kStagesRaw) & ~1;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kRingBytes +
                                     kMergeBytes + 2 * kStages * 8 + 64;
-  static_assert(kStages >= 2, "pipeline needs at least two stages");
+  static_assert(kStages >= 2 && kStages % 2 == 0,
+                "pipeline needs an even number (>= 2) of stages");
   static_assert(kSTiles % 2 == 0 && kPSteps >= 1, "warp tile shape");
+  static_assert(kQSteps % 2 == 0, "QK k-steps are split into two chains");
+  // Short accumulator chains: with few S tiles per warp the QK k-loop is
+  // split over two accumulator sets (even / odd k-steps) and summed.
+  static constexpr bool kSplitQK = kSTiles <= 4;
 };
 
 __device__ __forceinline__ int clamp_len(int L, int Smax) {
@@ -223,6 +238,104 @@ __device__ __forceinline__ long long block_incl_scan(long long v,
   return before + x;
 }
 
+// Issues the global loads of one unit's query rows into the mma A-fragment
+// registers qf (raw 16-bit pairs).  row0 / row1 are this thread's two fragment
+// rows; invalid rows read as zero.
+//
+// 16-bit cache: k-step ks uses d = 16ks + 2cq + {0,1} (+8), the layout of an
+// m16n8k16 A fragment.  FP8 cache: the k index is permuted so that each
+// thread's K bytes are one contiguous run of its token row: thread column cq
+// owns d in [cq*D/4, (cq+1)*D/4) and k-step ks uses d = cq*D/4 + 4ks + {0..3};
+// the raw pairs then go through fp8_finish_q.
+template <bool kFp8, int D, typename QT>
+__device__ __forceinline__ void load_q_raw(uint32_t (&qf)[D / 16][4],
+                                           const QT* q0, const QT* q1,
+                                           bool ok0, bool ok1, int cq) {
+  if constexpr (!kFp8) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int d0 = 16 * ks + 2 * cq;
+      qf[ks][0] = ok0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + d0)) : 0u;
+      qf[ks][1] = ok1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + d0)) : 0u;
+      qf[ks][2] = ok0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + d0 + 8)) : 0u;
+      qf[ks][3] = ok1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + d0 + 8)) : 0u;
+    }
+  } else {
+    // run of D/4 elements = D/2 bytes = D/32 16-byte vectors per row
+    const uint4* a = reinterpret_cast<const uint4*>(q0 + cq * (D / 4));
+    const uint4* b = reinterpret_cast<const uint4*>(q1 + cq * (D / 4));
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+      const uint4 va = ok0 ? __ldg(a + i) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 vb = ok1 ? __ldg(b + i) : make_uint4(0u, 0u, 0u, 0u);
+      // words 4i..4i+3 of the run: pairs (d, d+1) for d = 8i + {0, 2, 4, 6},
+      // i.e. k-steps 2i (words 4i, 4i+1) and 2i+1 (words 4i+2, 4i+3)
+      qf[2 * i][0] = va.x;
+      qf[2 * i][2] = va.y;
+      qf[2 * i + 1][0] = va.z;
+      qf[2 * i + 1][2] = va.w;
+      qf[2 * i][1] = vb.x;
+      qf[2 * i][3] = vb.y;
+      qf[2 * i + 1][1] = vb.z;
+      qf[2 * i + 1][3] = vb.w;
+    }
+  }
+}
+
+template <bool QBF16>
+__device__ __forceinline__ float2 unpack_q2(uint32_t w) {
+  if constexpr (QBF16) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+}
+
+// FP8 cache: turns the raw q pairs into f16 mma operands scaled by a power of
+// two that puts the largest |q| of the warp's rows in [2^14, 2^15) (exact, and
+// no q value can overflow f16).  Returns the exponent e of that power.
+template <bool QBF16, int D>
+__device__ __forceinline__ int fp8_finish_q(uint32_t (&qf)[D / 16][4]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 v = unpack_q2<QBF16>(qf[ks][i]);
+      amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
+    }
+  for (int off = 16; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  int e = 0;
+  if (amax > 0.f) {
+    int ex;
+    frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
+    e = 15 - ex;
+    e = e > 100 ? 100 : (e < -100 ? -100 : e);
+  }
+  const float up = ldexpf(1.f, e);
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 v = unpack_q2<QBF16>(qf[ks][i]);
+      qf[ks][i] = ptx::pack2<false>(v.x * up, v.y * up);
+    }
+  return e;
+}
+
+// Output column d of fragment element e of O n-tile n held by lane (cq = lane
+// & 3).  The FP8 path permutes columns so that its V bytes are contiguous.
+template <bool kFp8, int D>
+__device__ __forceinline__ int frag_col(int n, int e, int lane) {
+  const int cq = lane & 3;
+  if constexpr (!kFp8) {
+    return 8 * n + 2 * cq + (e & 1);
+  } else {
+    return (2 * cq + (e & 1)) * (D / 8) + n;
+  }
+}
+
 template <int KV, bool QBF16, int D, int HB>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap map_k,
@@ -247,7 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_b0;
   __shared__ int s_found;
   __shared__ volatile int s_abort;
-  __shared__ int s_last;
+  __shared__ float s_rowlse[HB * 16];   // log2-sum-exp per merged row
+  // Units this block covers only in part (at most the first and the last of
+  // its range); their split combine runs after the main loop.
+  __shared__ int s_pend_u[2], s_pend_b[2], s_pend_j[2], s_pend_cf[2],
+      s_pend_cl[2], s_pend_last[2];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -257,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], kConsumerWarps);
+      ptx::mbar_init(&empty[s], kGroupWarps);
     }
     ptx::fence_barrier_init();
     s_abort = 0;
@@ -267,36 +384,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- flat tile list: total N, this block's range, its first sequence ----
-  long long mine = 0;
-  for (int b = tid; b < p.B; b += kThreads)
-    mine += static_cast<long long>(
-                tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
-  const long long N = block_sum(mine, s_red);
-  // Blocks that take part: at most one per tile, so that every block in a
-  // unit's covering range [c_first, c_last] owns at least one of its tiles
-  // (the arrival count of the split combine relies on it).
-  const int P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
-  const long long t0 = cta < P ? N * cta / P : 0;
-  const long long t1 = cta < P ? N * (cta + 1) / P : 0;
-  if (t0 < t1) {
-    long long run = 0;
-    for (int base = 0; base < p.B; base += kThreads) {
-      const int b = base + tid;
-      long long v = 0;
-      if (b < p.B)
-        v = static_cast<long long>(
-                tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
-      long long tot;
-      const long long incl = block_incl_scan(v, s_red, &tot);
-      const long long excl = incl - v;
-      if (v > 0 && run + excl <= t0 && t0 < run + incl) {
-        s_b0 = b;
-        s_pref0 = run + excl;
-        s_found = 1;
+  // Blocks that take part: at most one per tile (P = min(grid, N)), so that
+  // every block in a unit's covering range [c_first, c_last] owns at least
+  // one of its tiles (the arrival count of the split combine relies on it).
+  long long N, t0 = 0, t1 = 0;
+  int P;
+  if (p.B <= kThreads) {
+    // one load of seq_lens and one block scan give everything
+    const int b = tid;
+    const long long v =
+        b < p.B ? static_cast<long long>(
+                      tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU
+                : 0;
+    const long long incl = block_incl_scan(v, s_red, &N);
+    P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
+    if (cta < P) {
+      t0 = N * cta / P;
+      t1 = N * (cta + 1) / P;
+    }
+    if (t0 < t1 && v > 0 && incl - v <= t0 && t0 < incl) {
+      s_b0 = b;
+      s_pref0 = incl - v;
+    }
+  } else {
+    long long mine = 0;
+    for (int b = tid; b < p.B; b += kThreads)
+      mine += static_cast<long long>(
+                  tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
+    N = block_sum(mine, s_red);
+    P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
+    if (cta < P) {
+      t0 = N * cta / P;
+      t1 = N * (cta + 1) / P;
+    }
+    if (t0 < t1) {
+      long long run = 0;
+      for (int base = 0; base < p.B; base += kThreads) {
+        const int b = base + tid;
+        long long v = 0;
+        if (b < p.B)
+          v = static_cast<long long>(
+                  tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
+        long long tot;
+        const long long incl = block_incl_scan(v, s_red, &tot);
+        const long long excl = incl - v;
+        if (v > 0 && run + excl <= t0 && t0 < run + incl) {
+          s_b0 = b;
+          s_pref0 = run + excl;
+          s_found = 1;
+        }
+        run += tot;
+        __syncthreads();
+        if (s_found) break;
       }
-      run += tot;
-      __syncthreads();
-      if (s_found) break;
     }
   }
   __syncthreads();
@@ -358,17 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ================================ consumers ===============================
-  const int cw = warp;                       // consumer warp 0..3
-  const int ct = tid;                        // consumer thread 0..127
-  const int hb = cw / C::kWarpsPerBlock;     // head block of this warp
-  const int wsl = cw % C::kWarpsPerBlock;    // token slice of this warp
+  const int cw = warp;                       // consumer warp 0..7
+  const int ct = tid;                        // consumer thread 0..255
+  const int grp = cw / kGroupWarps;          // ping-pong group
+  const int lw = cw % kGroupWarps;           // warp within the group
+  const int hb = lw / C::kWarpsPerBlock;     // head block of this warp
+  const int wsl = lw % C::kWarpsPerBlock;    // token slice of this warp
   const int r = lane >> 2, cq = lane & 3;    // mma fragment coordinates
 
   // Sequences with no valid token: all-zero output rows.
   for (int b = cta; b < p.B; b += gridDim.x) {
     if (clamp_len(__ldg(p.seq_lens + b), p.Smax) != 0) continue;
     const size_t base = static_cast<size_t>(b) * p.Hq * D;
-    for (int i = ct; i < p.Hq * D; i += kConsumerWarps * 32)
+    for (int i = ct; i < p.Hq * D; i += kConsumerThreads)
       store_out<QBF16>(p.out, base + i, 0.f);
   }
   if (t0 >= t1) return;
@@ -379,69 +521,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   float m[2], l[2];
   float s_mult = 0.f, o_mult = 1.f;
   bool fresh = true;
+  bool aborted = false;  // this warp gave up on a wait: skip further waits
+  // ticket of this block's arrival on a partly covered unit (thread 0 only)
+  uint32_t ticket0 = 0u, ticket1 = 0u;
+  int n_pend = 0;  // partly covered units met so far (at most 2)
+  if (ct == 0) s_pend_u[0] = s_pend_u[1] = -1;
+
+  // This thread's two fragment rows within its head block, and their query
+  // rows for unit (kvh, hc) of sequence b.
+  const int row0 = hb * 16 + r, row1 = row0 + 8;
+  auto issue_q = [&](int b, int kvh, int hc) {
+    const bool ok0 = row0 < p.R && hc * p.R + row0 < p.G;
+    const bool ok1 = row1 < p.R && hc * p.R + row1 < p.G;
+    const int h0 = kvh * p.G + hc * p.R + row0;
+    const QT* q0 = reinterpret_cast<const QT*>(p.q) +
+                   (static_cast<size_t>(b) * p.Hq + (ok0 ? h0 : 0)) * D;
+    const QT* q1 = reinterpret_cast<const QT*>(p.q) +
+                   (static_cast<size_t>(b) * p.Hq + (ok1 ? h0 + 8 : 0)) * D;
+    load_q_raw<kFp8, D, QT>(qf, q0, q1, ok0, ok1, cq);
+  };
+  issue_q(w.b, w.j / p.NHC, w.j % p.NHC);
 
   long long it = 0;
   for (long long g = t0; g < t1; ++g, ++it) {
     const int kvh = w.j / p.NHC, hc = w.j % p.NHC;
     if (fresh) {
-      // ---- new unit: query fragments, softmax state, multipliers ----
+      // ---- new unit: softmax state and multipliers (q already issued) ----
       fresh = false;
-      const int row0 = hb * 16 + r, row1 = row0 + 8;
-      const bool ok0 = row0 < p.R && hc * p.R + row0 < p.G;
-      const bool ok1 = row1 < p.R && hc * p.R + row1 < p.G;
-      const int h0 = kvh * p.G + hc * p.R + row0;
-      const int h1 = h0 + 8;
-      const QT* q0 = reinterpret_cast<const QT*>(p.q) +
-                     (static_cast<size_t>(w.b) * p.Hq + (ok0 ? h0 : 0)) * D;
-      const QT* q1 = reinterpret_cast<const QT*>(p.q) +
-                     (static_cast<size_t>(w.b) * p.Hq + (ok1 ? h1 : 0)) * D;
       if constexpr (!kFp8) {
-        // A fragment of k-step ks: (row r, d = 16ks + 2cq + {0,1}),
-        // (row r+8, same), (row r, +8), (row r+8, +8).
-#pragma unroll
-        for (int ks = 0; ks < C::kQSteps; ++ks) {
-          const int d0 = 16 * ks + 2 * cq;
-          qf[ks][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
-          qf[ks][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d0) : 0u;
-          qf[ks][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
-          qf[ks][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d0 + 8) : 0u;
-        }
         s_mult = p.scale_log2;
         o_mult = 1.f;
       } else {
-        // The k index of the QK product is permuted so that each thread's K
-        // bytes are one contiguous run of its token row: thread column cq owns
-        // d in [cq*D/4, (cq+1)*D/4); k-step ks uses d = cq*D/4 + 4ks + {0..3}.
-        constexpr int kRun = D / 4;
-        float qa[kRun], qb[kRun];
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < kRun; ++i) {
-          qa[i] = ok0 ? to_f32<QT>(q0[cq * kRun + i]) : 0.f;
-          qb[i] = ok1 ? to_f32<QT>(q1[cq * kRun + i]) : 0.f;
-          amax = fmaxf(amax, fmaxf(fabsf(qa[i]), fabsf(qb[i])));
-        }
-        for (int off = 16; off > 0; off >>= 1)
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        // Power of two putting the largest |q| in [2^14, 2^15): exact, and
-        // no q value can overflow f16.
-        int e = 0;
-        if (amax > 0.f) {
-          int ex;
-          frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
-          e = 15 - ex;
-          e = e > 100 ? 100 : (e < -100 ? -100 : e);
-        }
-        const float up = ldexpf(1.f, e);
-#pragma unroll
-        for (int ks = 0; ks < C::kQSteps; ++ks) {
-          qf[ks][0] = ptx::pack2<false>(qa[4 * ks] * up, qa[4 * ks + 1] * up);
-          qf[ks][1] = ptx::pack2<false>(qb[4 * ks] * up, qb[4 * ks + 1] * up);
-          qf[ks][2] = ptx::pack2<false>(qa[4 * ks + 2] * up,
-                                        qa[4 * ks + 3] * up);
-          qf[ks][3] = ptx::pack2<false>(qb[4 * ks + 2] * up,
-                                        qb[4 * ks + 3] * up);
-        }
+        const int e = fp8_finish_q<QBF16, D>(qf);
         const int sidx = w.b * p.Hkv + kvh;
         s_mult = p.scale_log2 * __ldg(p.k_scale + sidx) * ldexpf(1.f, -e);
         o_mult = __ldg(p.v_scale + sidx);
@@ -453,12 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       l[0] = l[1] = 0.f;
     }
 
-    // ---- wait for the stage ----
+    if ((it & 1) == grp) {
+    // ---- wait for the stage (tiles alternate between the two groups) ----
     const int stage = static_cast<int>(it % C::kStages);
     const uint32_t ph = static_cast<uint32_t>((it / C::kStages) & 1);
-    if (!s_abort && !ptx::mbar_wait_bounded(&full[stage], ph, kWaitLimitNs)) {
+    if (!aborted && !ptx::mbar_wait_bounded(&full[stage], ph, kWaitLimitNs)) {
       atomicOr(p.error, kErrWaitTimeout);
-      s_abort = 1;
+      aborted = true;
+      s_abort = 1;  // stops the producer
     }
     const uint32_t kbase = ptx::smem_u32(ring + stage * C::kStageBytes);
     const uint32_t vbase = kbase + C::kTileBytes;
@@ -469,8 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- S = Q K^T for this warp's tokens ----
     float s[C::kSTiles][4];
+    float s2[C::kSplitQK ? C::kSTiles : 1][4];  // odd k-steps when split
 #pragma unroll
     for (int n = 0; n < C::kSTiles; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int n = 0; n < (C::kSplitQK ? C::kSTiles : 1); ++n)
+      s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.f;
 
     if constexpr (!kFp8) {
       const int mi = lane >> 3, rr = lane & 7;
@@ -482,8 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int chunk = 2 * ks + (mi & 1);
           uint32_t b0, b1, b2, b3;
           ptx::ldsm_x4(kbase + swz16(t, chunk), b0, b1, b2, b3);
-          ptx::mma16816<kMmaBF16>(s[2 * np], qf[ks], b0, b1);
-          ptx::mma16816<kMmaBF16>(s[2 * np + 1], qf[ks], b2, b3);
+          if (C::kSplitQK && (ks & 1)) {
+            ptx::mma16816<kMmaBF16>(s2[2 * np], qf[ks], b0, b1);
+            ptx::mma16816<kMmaBF16>(s2[2 * np + 1], qf[ks], b2, b3);
+          } else {
+            ptx::mma16816<kMmaBF16>(s[2 * np], qf[ks], b0, b1);
+            ptx::mma16816<kMmaBF16>(s[2 * np + 1], qf[ks], b2, b3);
+          }
         }
       }
     } else {
@@ -504,8 +626,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < C::kQSteps; ++ks) {
           const uint32_t b0 = ptx::e4m3x2_to_f16x2(kw[ks] & 0xffffu);
           const uint32_t b1 = ptx::e4m3x2_to_f16x2(kw[ks] >> 16);
-          ptx::mma16816<false>(s[n], qf[ks], b0, b1);
+          if (C::kSplitQK && (ks & 1))
+            ptx::mma16816<false>(s2[n], qf[ks], b0, b1);
+          else
+            ptx::mma16816<false>(s[n], qf[ks], b0, b1);
         }
+      }
+    }
+    if constexpr (C::kSplitQK) {
+#pragma unroll
+      for (int n = 0; n < C::kSTiles; ++n) {
+        s[n][0] += s2[n][0];
+        s[n][1] += s2[n][1];
+        s[n][2] += s2[n][2];
+        s[n][3] += s2[n][3];
       }
     }
 
@@ -651,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- release the stage ----
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&empty[stage]);
+    }  // this group's tile
 
     const bool unit_end = (w.ti == w.nt - 1) || (g == t1 - 1);
     if (unit_end) {
@@ -660,28 +795,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c_first = block_of_tile(us, N, P);
       const int c_last = block_of_tile(us + w.nt - 1, N, P);
       const bool whole = (c_first == c_last);
+      const int bq = w.b;
+      // The next unit's query rows load while this epilogue runs (qf is dead
+      // after the unit's last QK^T).
+      if (g + 1 < t1) {
+        TileWalk wn = w;
+        wn.next(p, HU);
+        issue_q(wn.b, wn.j / p.NHC, wn.j % p.NHC);
+      }
 
-      // 1) this warp's state -> shared memory, canonical [row][d] layout
+      // 1) this warp's state -> shared memory in mma fragment order
+      //    (position (n*4 + e)*32 + lane: conflict-free), valid rows only
       float lt0 = l[0], lt1 = l[1];
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 1);
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 1);
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+      const bool hi_rows = hb * 16 + 8 < p.R;  // rows r+8 exist (uniform)
       float* mo = mrg_o + cw * 16 * D;
 #pragma unroll
       for (int n = 0; n < C::kOTiles; ++n) {
-        int d0, d1;
-        if constexpr (!kFp8) {
-          d0 = 8 * n + 2 * cq;
-          d1 = d0 + 1;
-        } else {
-          d0 = (2 * cq) * (D / 8) + n;
-          d1 = (2 * cq + 1) * (D / 8) + n;
+        mo[(n * 4 + 0) * 32 + lane] = o[n][0];
+        mo[(n * 4 + 1) * 32 + lane] = o[n][1];
+        if (hi_rows) {
+          mo[(n * 4 + 2) * 32 + lane] = o[n][2];
+          mo[(n * 4 + 3) * 32 + lane] = o[n][3];
         }
-        mo[r * D + d0] = o[n][0];
-        mo[r * D + d1] = o[n][1];
-        mo[(r + 8) * D + d0] = o[n][2];
-        mo[(r + 8) * D + d1] = o[n][3];
       }
       if (cq == 0) {
         mrg_m[cw * 16 + r] = m[0];
@@ -689,80 +828,165 @@ __global__ void __launch_bounds__(kThreads, 1)
         mrg_l[cw * 16 + r] = lt0;
         mrg_l[cw * 16 + r + 8] = lt1;
       }
-      ptx::named_bar_sync(1, kConsumerWarps * 32);
+      ptx::named_bar_sync(1, kConsumerThreads);
 
-      // 2) merge the warps of each head block; write out or write a partial
-      const int slot = c_first == c_last ? 0 : cta + u;
-      for (int idx = ct; idx < C::kRowsPad * D; idx += kConsumerWarps * 32) {
-        const int row = idx / D, d = idx % D;
-        if (row >= p.R || hc * p.R + row >= p.G) continue;
-        const int hbk = row >> 4, rr = row & 15;
+      // 2) per merged row: the max over warps, the total, and each warp's
+      //    weight exp2(m_w - M) / total (written over m_w)
+      if (ct < HB * 16) {
+        const int hbk = ct >> 4, rr = ct & 15;
         float M = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < C::kWarpsPerBlock; ++k)
-          M = fmaxf(M, mrg_m[(hbk * C::kWarpsPerBlock + k) * 16 + rr]);
-        const float Mb = (M == -INFINITY) ? 0.f : M;
-        float lt = 0.f, acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < C::kWarpsPerBlock; ++k) {
-          const int wk = hbk * C::kWarpsPerBlock + k;
-          const float f = ptx::ex2(mrg_m[wk * 16 + rr] - Mb);
-          lt += mrg_l[wk * 16 + rr] * f;
-          acc += mrg_o[(wk * 16 + rr) * D + d] * f;
+        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
+          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
+                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
+          M = fmaxf(M, mrg_m[wk * 16 + rr]);
         }
-        const float val = lt > 0.f ? acc / lt : 0.f;
+        const float Mb = (M == -INFINITY) ? 0.f : M;
+        float lt = 0.f;
+        float f[kGroups * C::kWarpsPerBlock];
+#pragma unroll
+        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
+          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
+                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
+          f[k] = ptx::ex2(mrg_m[wk * 16 + rr] - Mb);
+          lt += mrg_l[wk * 16 + rr] * f[k];
+        }
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
+          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
+                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
+          mrg_m[wk * 16 + rr] = f[k] * inv;
+        }
+        s_rowlse[ct] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
+      }
+      ptx::named_bar_sync(1, kConsumerThreads);
+
+      // 3) merge position by position; write the output rows (unit covered by
+      //    this block alone) or the normalised partial ([row][d], fp32)
+      const int slot = whole ? 0 : cta + u;
+      constexpr int kPos = C::kOTiles * 4 * 32;  // positions per head block
+      for (int idx = ct; idx < HB * kPos; idx += kConsumerThreads) {
+        const int hbk = idx / kPos, pos = idx % kPos;
+        const int n = pos >> 7, e = (pos >> 5) & 3, ln = pos & 31;
+        const int rr = (ln >> 2) + 8 * (e >> 1);
+        const int row = hbk * 16 + rr;
+        if (row >= p.R || hc * p.R + row >= p.G) continue;  // warp-uniform
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
+          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
+                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
+          acc += mrg_m[wk * 16 + rr] * mrg_o[wk * 16 * D + pos];
+        }
         if (whole) {
           const int h = kvh * p.G + hc * p.R + row;
           store_out<QBF16>(p.out,
-                           (static_cast<size_t>(w.b) * p.Hq + h) * D + d,
-                           val * o_mult);
+                           (static_cast<size_t>(bq) * p.Hq + h) * D +
+                               frag_col<kFp8, D>(n, e, ln),
+                           acc * o_mult);
         } else {
-          const size_t prow = static_cast<size_t>(slot) * C::kRowsPad + row;
-          p.part_o[prow * D + d] = val;
-          if (d == 0) p.part_lse[prow] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
+          p.part_o[(static_cast<size_t>(slot) * C::kRowsPad + row) * D +
+                   frag_col<kFp8, D>(n, e, ln)] = acc;
         }
       }
+      if (!whole && ct < HB * 16)
+        p.part_lse[static_cast<size_t>(slot) * C::kRowsPad + ct] = s_rowlse[ct];
+      ptx::named_bar_sync(1, kConsumerThreads);
 
-      if (!whole) {
-        // 3) count arrivals; the last block of the unit combines the partials
-        __threadfence();
-        ptx::named_bar_sync(1, kConsumerWarps * 32);
+      // 4) partial: count this block's arrival (release: all the block's
+      //    partial stores are ordered before it by the barrier and the
+      //    fence); whether this block is the unit's last arrival is only
+      //    looked at after the main loop
+      if (!whole && n_pend < 2) {
         if (ct == 0) {
-          const uint32_t n_cover = static_cast<uint32_t>(c_last - c_first + 1);
-          const uint32_t ticket = atomicAdd(p.counters + u, 1u);
-          s_last = (ticket == n_cover - 1) ? 1 : 0;
-        }
-        ptx::named_bar_sync(1, kConsumerWarps * 32);
-        if (s_last) {
           __threadfence();
-          for (int idx = ct; idx < C::kRowsPad * D;
-               idx += kConsumerWarps * 32) {
-            const int row = idx / D, d = idx % D;
-            if (row >= p.R || hc * p.R + row >= p.G) continue;
-            float M = -INFINITY;
-            for (int c = c_first; c <= c_last; ++c)
-              M = fmaxf(M, __ldcg(p.part_lse +
-                                  static_cast<size_t>(c + u) * C::kRowsPad + row));
-            const float Mb = (M == -INFINITY) ? 0.f : M;
-            float lt = 0.f, acc = 0.f;
-            for (int c = c_first; c <= c_last; ++c) {
-              const size_t prow = static_cast<size_t>(c + u) * C::kRowsPad + row;
-              const float f = ptx::ex2(__ldcg(p.part_lse + prow) - Mb);
-              lt += f;
-              acc += f * __ldcg(p.part_o + prow * D + d);
-            }
-            const int h = kvh * p.G + hc * p.R + row;
-            store_out<QBF16>(p.out,
-                             (static_cast<size_t>(w.b) * p.Hq + h) * D + d,
-                             (lt > 0.f ? acc / lt : 0.f) * o_mult);
-          }
-          if (ct == 0) p.counters[u] = 0u;
+          const uint32_t t = atomicAdd(p.counters + u, 1u);
+          if (n_pend == 0) ticket0 = t; else ticket1 = t;
+          s_pend_u[n_pend] = u;
+          s_pend_b[n_pend] = bq;
+          s_pend_j[n_pend] = w.j;
+          s_pend_cf[n_pend] = c_first;
+          s_pend_cl[n_pend] = c_last;
         }
+        ++n_pend;
       }
-      ptx::named_bar_sync(1, kConsumerWarps * 32);
       fresh = true;
     }
     w.next(p, HU);
+  }
+
+  // ---- split combine of the units whose last arrival was this block ----
+  if (ct == 0) {
+    s_pend_last[0] = n_pend > 0 &&
+        ticket0 == static_cast<uint32_t>(s_pend_cl[0] - s_pend_cf[0]);
+    s_pend_last[1] = n_pend > 1 &&
+        ticket1 == static_cast<uint32_t>(s_pend_cl[1] - s_pend_cf[1]);
+    __threadfence();  // acquire: other blocks' partials before the reads below
+  }
+  ptx::named_bar_sync(1, kConsumerThreads);
+  for (int i = 0; i < 2; ++i) {
+    if (!s_pend_last[i]) continue;  // uniform
+    const int u = s_pend_u[i], b = s_pend_b[i], j = s_pend_j[i];
+    const int kvh = j / p.NHC, hc = j % p.NHC;
+    const int cf = s_pend_cf[i], cl = s_pend_cl[i];
+    const float om = kFp8 ? __ldg(p.v_scale + b * p.Hkv + kvh) : 1.f;
+    // valid rows of this head chunk, row-major elements (row, d)
+    const int rows = min(p.R, p.G - hc * p.R);
+    const int nv = rows * D;
+    const size_t h_base =
+        (static_cast<size_t>(b) * p.Hq + kvh * p.G + hc * p.R) * D;
+    // Four elements per thread at a time, four partials per batch, all
+    // loads in flight together; running maximum across batches.
+    constexpr int kE = 4, kB = 4;
+    for (int v0 = ct; v0 < nv; v0 += kE * kConsumerThreads) {
+      float M[kE], lt[kE], acc[kE];
+#pragma unroll
+      for (int x = 0; x < kE; ++x) {
+        M[x] = -INFINITY;
+        lt[x] = 0.f;
+        acc[x] = 0.f;
+      }
+      for (int c0 = cf; c0 <= cl; c0 += kB) {
+        float ls[kB][kE], ov[kB][kE];
+#pragma unroll
+        for (int k = 0; k < kB; ++k)
+#pragma unroll
+          for (int x = 0; x < kE; ++x) {
+            const int v = v0 + x * kConsumerThreads;
+            const bool ok = c0 + k <= cl && v < nv;
+            const size_t sl = static_cast<size_t>(c0 + k + u);
+            ls[k][x] = ok ? __ldcg(p.part_lse + sl * C::kRowsPad + v / D)
+                          : -INFINITY;
+            ov[k][x] = ok ? __ldcg(p.part_o + sl * C::kRowsPad * D + v) : 0.f;
+          }
+#pragma unroll
+        for (int x = 0; x < kE; ++x) {
+          const float Mn =
+              fmaxf(M[x], fmaxf(fmaxf(ls[0][x], ls[1][x]),
+                                fmaxf(ls[2][x], ls[3][x])));
+          if (Mn == -INFINITY) continue;
+          const float a = ptx::ex2(M[x] - Mn);  // 0 while M is -inf
+          lt[x] *= a;
+          acc[x] *= a;
+#pragma unroll
+          for (int k = 0; k < kB; ++k) {
+            const float f = ptx::ex2(ls[k][x] - Mn);
+            lt[x] += f;
+            acc[x] += f * ov[k][x];
+          }
+          M[x] = Mn;
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < kE; ++x) {
+        const int v = v0 + x * kConsumerThreads;
+        if (v < nv)
+          store_out<QBF16>(p.out, h_base + v,
+                           (lt[x] > 0.f ? acc[x] / lt[x] : 0.f) * om);
+      }
+    }
+    if (ct == 0) p.counters[u] = 0u;
   }
 }
 

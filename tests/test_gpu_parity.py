@@ -54,6 +54,11 @@ CASES = [
     ("fp8_f16_q_g4", 2, 16, 4, 128, 150, "f16", "e4m3", ("list", 150, 80)),
     ("fp8_mqa_g64", 1, 64, 1, 128, 300, "bf16", "e4m3", ("uniform",)),
     ("fp8_mha_g1", 2, 4, 4, 64, 99, "bf16", "e4m3", ("list", 99, 17)),
+    # more sequences than threads per block: the general scheduler prologue
+    ("bf16_many_sequences", 300, 8, 2, 64, 70, "bf16", "same",
+     ("ragged", 0, 70)),
+    ("fp8_many_sequences", 290, 8, 2, 128, 80, "bf16", "e4m3",
+     ("ragged", 0, 80)),
 ]
 
 
