@@ -11,6 +11,8 @@ its names:
 * :func:`gqa_decode` — one decode step with a float16 / bfloat16 cache;
 * :func:`gqa_decode_fp8` — the same with an FP8 E4M3 cache and per-(sequence,
   KV head) scales;
+* :func:`gqa_decode_static` — gqa_decode with a fixed scratch array instead of
+  any device allocation;
 * :func:`gqa_kv_bytes_per_token`, :func:`gqa_status_string`,
   :func:`gqa_device_errors`, :func:`gqa_set_num_ctas`,
   :func:`gqa_last_launch_count`.
@@ -35,6 +37,8 @@ SIGNATURES = {
                           _I32, _I32, _I32, _VP]),
     "gqa_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
                               _I32, _I32, _I32, _I32, _I32, _VP]),
+    "gqa_decode_static": (_I32, [_VP, _VP, _VP, _VP, _F32, _VP, _I32, _I32,
+                                 _I32, _I32, _I32, _I32, _VP]),
     "gqa_kv_bytes_per_token": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "gqa_status_string": (ctypes.c_char_p, [_I32]),
     "gqa_device_errors": (_I32, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
@@ -148,6 +152,36 @@ def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out=None,
                           _stream_handle(stream))
     if st != GQA_OK:
         raise GQAError(st, "gqa_decode")
+    return out
+
+
+def gqa_decode_static(q, k_cache, v_cache, seq_lens, scale: float, out=None,
+                      stream=None):
+    """gqa_decode that allocates no device memory (fixed 16 MiB scratch kept
+    by the library on each GPU); for callers that must not let the library
+    allocate while they run.  ``out`` must be given by such callers (a new
+    tensor is only created here when it is None).  Calls that overlap on the
+    GPU share the scratch and race: keep them ordered."""
+    import torch
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("seq_lens", seq_lens)):
+        _check_dev(n, t)
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, k_cache and v_cache must share a dtype")
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    B, Hq, D = q.shape
+    _, Hkv, Smax, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_dev("out", out)
+    st = lib().gqa_decode_static(q.data_ptr(), k_cache.data_ptr(),
+                                 v_cache.data_ptr(), seq_lens.data_ptr(),
+                                 float(scale), out.data_ptr(), B, Hq, Hkv,
+                                 Smax, D, _dtype_code(q),
+                                 _stream_handle(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_decode_static")
     return out
 
 

@@ -289,6 +289,115 @@ gqa_status launch(const void* q, const void* k, const void* v,
 }  // namespace
 }  // namespace gqa
 
+// ------------------------------------------------- fixed-scratch variant
+//
+// Scratch of gqa_decode_static: one array per GPU in the library's static
+// device memory, [error word | arrival counters | partial log2-sum-exp |
+// partial O].  It exists on every device that loads the library until the
+// process exits, so its size is kept modest.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t gqa_static_scratch[kStaticScratchBytes];
+
+namespace gqa {
+namespace {
+
+// Device address of gqa_static_scratch, looked up once per device (with
+// that device current).  The host-side name of the array is only a stand-in:
+// a kernel must be given this address instead.
+std::map<int, void*> g_static_addr;
+
+cudaError_t static_scratch_addr(int dev, void** out) {
+  auto it = g_static_addr.find(dev);
+  if (it != g_static_addr.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, gqa_static_scratch);
+  if (e != cudaSuccess) return e;
+  g_static_addr.emplace(dev, ptr);
+  *out = ptr;
+  return cudaSuccess;
+}
+
+// Same plan and kernel as launch(), with the scratch carved out of
+// gqa_static_scratch instead of the per-stream allocation.
+gqa_status launch_static(const void* q, const void* k, const void* v,
+                         const int32_t* seq_lens, float scale, void* out,
+                         int B, int Hq, int Hkv, int Smax, int D, int kv_kind,
+                         bool q_bf16, void* stream_ptr) {
+  t_last_launches = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int G = Hq / Hkv;
+  const int NHC = (G + kMaxUnitRows - 1) / kMaxUnitRows;
+  const int R = (G + NHC - 1) / NHC;
+  const int hb = R <= 16 ? 1 : (R <= 32 ? 2 : 4);
+  const int rows_pad = hb * 16;
+  const long long units = static_cast<long long>(B) * Hkv * NHC;
+  if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
+
+  const Variant var = pick(kv_kind, q_bf16, D, hb);
+  CUtensorMap map_k, map_v;
+  if (!make_cache_map(&map_k, k, 2, B, Hkv, Smax, D) ||
+      !make_cache_map(&map_v, v, 2, B, Hkv, Smax, D))
+    return GQA_ERR_CUDA;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  int sms = 0, per_sm = 0;
+  if (configure(dev, var, &sms, &per_sm) != cudaSuccess) return GQA_ERR_CUDA;
+  const long long max_tiles =
+      units * ((static_cast<long long>(Smax) + kTileTokens - 1) / kTileTokens);
+  const long long wave = static_cast<long long>(sms) * per_sm;
+  const int grid = g_num_ctas_override > 0
+                       ? g_num_ctas_override
+                       : static_cast<int>(max_tiles < wave ? max_tiles : wave);
+
+  const size_t slots = static_cast<size_t>(grid) + static_cast<size_t>(units);
+  const size_t cnt_bytes = align_up(static_cast<size_t>(units) * 4, 256);
+  const size_t lse_bytes = align_up(slots * rows_pad * 4, 256);
+  const size_t o_bytes = slots * rows_pad * static_cast<size_t>(D) * 4;
+  const size_t need = kHeaderBytes + cnt_bytes + lse_bytes + o_bytes;
+  if (need > kStaticScratchBytes) return GQA_ERR_UNSUPPORTED;
+
+  void* base = nullptr;
+  if (static_scratch_addr(dev, &base) != cudaSuccess) return GQA_ERR_CUDA;
+  uint8_t* wb = static_cast<uint8_t*>(base);
+  // The array keeps whatever the previous call left: the error word and the
+  // arrival counters must start at zero.
+  if (cudaMemsetAsync(wb, 0, kHeaderBytes + cnt_bytes, stream) != cudaSuccess)
+    return GQA_ERR_CUDA;
+
+  DecodeParams p;
+  p.q = q;
+  p.out = out;
+  p.seq_lens = seq_lens;
+  p.k_scale = nullptr;
+  p.v_scale = nullptr;
+  p.error = reinterpret_cast<uint32_t*>(wb);
+  p.counters = reinterpret_cast<uint32_t*>(wb + kHeaderBytes);
+  p.part_lse = reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes);
+  p.part_o =
+      reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes + lse_bytes);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Smax = Smax;
+  p.G = G;
+  p.NHC = NHC;
+  p.R = R;
+
+  var.fn<<<grid, kThreads, var.smem, stream>>>(map_k, map_v, p);
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  t_last_launches = 1;
+  return GQA_OK;
+}
+
+}  // namespace
+}  // namespace gqa
+
 extern "C" {
 
 gqa_status gqa_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -374,6 +483,25 @@ gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
 void gqa_set_num_ctas(int num_ctas) {
   std::lock_guard<std::mutex> lock(gqa::g_mu);
   gqa::g_num_ctas_override = num_ctas > 0 ? num_ctas : 0;
+}
+
+gqa_status gqa_decode_static(const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* seq_lens,
+                             float scale, void* out, int B, int Hq, int Hkv,
+                             int Smax, int D, gqa_dtype dtype, void* stream) {
+  gqa::t_last_launches = 0;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  const gqa_status st = gqa::check_common(q, k_cache, v_cache, seq_lens, scale,
+                                          out, B, Hq, Hkv, Smax, D);
+  if (st != GQA_OK) return st;
+  try {
+    return gqa::launch_static(q, k_cache, v_cache, seq_lens, scale, out, B, Hq,
+                              Hkv, Smax, D,
+                              dtype == GQA_BF16 ? gqa::kKvBF16 : gqa::kKvF16,
+                              dtype == GQA_BF16, stream);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
 }
 
 int gqa_last_launch_count(void) { return gqa::t_last_launches; }

@@ -116,6 +116,42 @@ gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
                           int Smax, int D, gqa_dtype qo_dtype, void* stream);
 
 /*
+ * gqa_decode_static — gqa_decode without any device allocation.
+ *
+ * The pages have no counterpart to this call.  It is for callers that cannot
+ * let a library allocate GPU memory while it runs: serving engines that
+ * reserve the device's memory for their own pool at start-up and allow no
+ * allocation behind their back afterwards, and latency-critical decode loops
+ * in which an allocation could stall or fail at the wrong moment.  gqa_decode
+ * keeps a growable scratch buffer per stream that it allocates on first use;
+ * this entry point instead takes its scratch (the split partial results and
+ * their arrival counters) from one fixed 16 MiB array that the library keeps
+ * in static device memory on every GPU that loads it, until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, layout, numerics and errors: as gqa_decode; the caller provides
+ * every input and the output.  In addition:
+ *  - Size limit.  A request whose scratch does not fit in the 16 MiB array
+ *    returns GQA_ERR_UNSUPPORTED before anything is enqueued.  The scratch
+ *    is about (blocks + B*Hkv*ceil(G/64)) x rows x D x 4 bytes, rows = 16, 32
+ *    or 64 by G: e.g. B=8, Hq=64, Hkv=8, D=128 needs about 1.8 MB on a
+ *    148-SM GPU, while B=32, Hq=Hkv=64, D=128 needs 18 MB and is refused.
+ *  - Set-up.  The first call on each device looks up the device address of
+ *    the array (once per device, with that device current).  Make that first
+ *    call before any stream capture.
+ *  - Sharing.  Every call on a device uses the same array, which keeps what
+ *    the previous call left in it; each call first clears the part that must
+ *    start at zero (an asynchronous memset on `stream`, then the kernel).
+ *    Calls whose execution overlaps on the GPU (e.g. on two streams with no
+ *    ordering between them) race on the array and give wrong results.
+ *  - Fault flags raised by its kernel are not reported by gqa_device_errors.
+ */
+gqa_status gqa_decode_static(const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* seq_lens,
+                             float scale, void* out, int B, int Hq, int Hkv,
+                             int Smax, int D, gqa_dtype dtype, void* stream);
+
+/*
  * gqa_kv_bytes_per_token — KV-cache bytes one token occupies across a model:
  * 2 (K and V) x layers x kv_heads x head_dim x bytes_per_elem ("Grouped Query
  * Attention: Why 8 KV Heads Decide Your Batch Size", TL;DR; e.g. 327,680 B =
