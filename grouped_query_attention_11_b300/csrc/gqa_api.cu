@@ -280,8 +280,23 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.NHC = NHC;
   p.R = R;
 
-  var.fn<<<grid, kThreads, var.smem, stream>>>(map_k, map_v, p);
-  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  // Programmatic dependent launch: the kernel may start launching while the
+  // previous kernel in the stream finishes; it waits (griddepcontrol.wait)
+  // for that kernel's completion before it reads any global memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = var.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, var.fn, map_k, map_v, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
   t_last_launches = 1;
   return GQA_OK;
 }

@@ -17,7 +17,12 @@
 //    contiguous tile range [c*N/P, (c+1)*N/P).  Every block streams the same
 //    number of KV bytes (+-1 tile), whatever the length mix.  A unit cut by a
 //    range boundary is finished by the fused split combine below.
-//  * KV stream.  One producer warp issues TMA tensor loads (128-byte
+//  * Warp roles.  A block is three warpgroups.  Warpgroup 0: one producer
+//    warp and three merge warps; warpgroups 1 and 2: the two ping-pong
+//    consumer groups.  setmaxnreg moves registers from warpgroup 0 (56 per
+//    thread) to the consumers (224), whose mma fragments, accumulators and
+//    query rows then never spill.
+//  * KV stream.  The producer warp issues TMA tensor loads (128-byte
 //    swizzle, L2 evict-first) of the K and V tiles into a multi-stage shared
 //    memory ring guarded by mbarriers.  Each KV byte is read from HBM once and
 //    serves all query heads of its group from shared memory.
@@ -28,18 +33,22 @@
 //    reductions are two quad shuffles.
 //  * Ping-pong consumers.  Two groups of four consumer warps take alternate
 //    ring stages, each with its own softmax state, so that one group's
-//    dependent mma / exp chains overlap the other's; the states of both groups
-//    merge at the end of every unit.
+//    dependent mma / exp chains overlap the other's.
+//  * Asynchronous unit epilogue.  At the end of a unit every consumer warp
+//    only dumps its softmax state to shared memory (mma fragment order) and
+//    signals an mbarrier; it goes straight on with the next unit, whose query
+//    rows it has already started loading.  The merge warps combine the eight
+//    states, write the output rows or a split partial, and publish the
+//    block's arrival, off the consumers' critical path.
 //  * FP8 E4M3 cache.  Bytes are turned into exact f16 pairs in registers
 //    (cvt.rn.f16x2.e4m3x2); q is moved into f16 with a per-head-block power
 //    of two so no value can overflow; k_scale and the power of two fold into
 //    the score multiplier and v_scale into the output.
-//  * Split combine.  Warps of a block merge through shared memory.  A unit
-//    covered by one block is written out directly; otherwise each block
-//    writes a normalised partial (O, log2-sum-exp) and bumps a per-unit
-//    counter; the block that arrives last merges all partials of the unit and
-//    writes the output, then resets the counter.  No block ever waits on
-//    another block.
+//  * Split combine.  A unit covered by one block is written out directly;
+//    otherwise each block writes a normalised partial (O, log2-sum-exp) and
+//    bumps a per-unit counter; the block that arrives last merges all
+//    partials of the unit (after its own last unit) and writes the output,
+//    then resets the counter.  No block ever waits on another block.
 //  * Every mbarrier wait gives up after a time limit, sets an error flag the
 //    host can query, and lets the block finish without hanging the GPU.
 #pragma once
@@ -61,11 +70,24 @@ constexpr int kGroupWarps = 4;     // consumer warps per ping-pong group
 constexpr int kGroups = 2;         // groups taking alternate ring stages
 constexpr int kConsumerWarps = kGroups * kGroupWarps;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kMergeWarps = 3;     // warps 1..3 of warpgroup 0
+constexpr int kMergeThreads = kMergeWarps * 32;
+constexpr int kFirstConsumerWarp = 4;
+constexpr int kThreads = 3 * 128;  // three warpgroups
+// Registers per thread after the setmaxnreg split: warpgroup 0 gives up
+// registers to the two consumer warpgroups.  The sum equals the launch's
+// total (384 threads x 168, the __launch_bounds__(384, 1) allocation):
+// 128 x 56 + 256 x 224 = 64512.
+constexpr int kRegsSmall = 56;
+constexpr int kRegsBig = 224;
+static_assert(128 * kRegsSmall + 256 * kRegsBig <= kThreads * 168,
+              "register split exceeds the launch allocation");
 constexpr int kMaxUnitRows = 64;  // query heads per unit (4 head blocks)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
-constexpr int kSmemBudget = 220 * 1024;
+// Dynamic shared memory per block: the sm_100-family opt-in maximum (227 KB)
+// less 1 KB left for the kernel's static shared variables.
+constexpr int kSmemBudget = 232448 - 1024;
 
 enum KvKind : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
 
@@ -336,6 +358,148 @@ __device__ __forceinline__ int frag_col(int n, int e, int lane) {
   }
 }
 
+// Merges the eight consumer warps' dumped softmax states of one unit
+// (warps of head block hbk: both groups' warps with that head block) and
+// writes the unit's output rows (whole: the unit lies in this block alone) or
+// its normalised partial (row-major fp32 + log2-sum-exp per row).  Run by
+// kNT threads (t = 0 .. kNT-1) that synchronise on named barrier kBar.
+template <int KV, bool QBF16, int D, int HB, int kNT, int kBar>
+__device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
+                                           float* dmp_m, const float* dmp_l,
+                                           float* s_rowlse,
+                                           const DecodeParams& p, int u,
+                                           int bq, int j, bool whole, int cta) {
+  using C = Cfg<KV, D, HB>;
+  constexpr bool kFp8 = (KV == kKvE4M3);
+  constexpr int kPos = C::kOTiles * 4 * 32;  // fragment positions per warp
+  constexpr int kW = kGroups * C::kWarpsPerBlock;  // warps per head block
+  const int kvh = j / p.NHC, hc = j % p.NHC;
+  const float o_mult = kFp8 ? __ldg(p.v_scale + bq * p.Hkv + kvh) : 1.f;
+  // the k-th warp of head block hbk
+  auto warp_of = [](int hbk, int k) {
+    return (k / C::kWarpsPerBlock) * kGroupWarps + hbk * C::kWarpsPerBlock +
+           k % C::kWarpsPerBlock;
+  };
+
+  // 1) per merged row: the max over the head block's warps, the total, and
+  //    each warp's weight exp2(m_w - M) / total (written over m_w)
+  for (int row = t; row < HB * 16; row += kNT) {
+    const int hbk = row >> 4, rr = row & 15;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kW; ++k) M = fmaxf(M, dmp_m[warp_of(hbk, k) * 16 + rr]);
+    const float Mb = (M == -INFINITY) ? 0.f : M;
+    float lt = 0.f;
+    float f[kW];
+#pragma unroll
+    for (int k = 0; k < kW; ++k) {
+      const int wk = warp_of(hbk, k);
+      f[k] = ptx::ex2(dmp_m[wk * 16 + rr] - Mb);
+      lt += dmp_l[wk * 16 + rr] * f[k];
+    }
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+    for (int k = 0; k < kW; ++k) dmp_m[warp_of(hbk, k) * 16 + rr] = f[k] * inv;
+    s_rowlse[row] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
+  }
+  ptx::named_bar_sync(kBar, kNT);
+
+  // 2) merge position by position (positions of one warp-sized run share
+  //    (n, e), so the row test below is uniform across a warp)
+  const int slot = whole ? 0 : cta + u;
+  for (int idx = t; idx < HB * kPos; idx += kNT) {
+    const int hbk = idx / kPos, pos = idx % kPos;
+    const int n = pos >> 7, e = (pos >> 5) & 3, ln = pos & 31;
+    const int rr = (ln >> 2) + 8 * (e >> 1);
+    const int row = hbk * 16 + rr;
+    if (row >= p.R || hc * p.R + row >= p.G) continue;
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < kW; ++k) {
+      const int wk = warp_of(hbk, k);
+      acc += dmp_m[wk * 16 + rr] * dmp_o[wk * 16 * D + pos];
+    }
+    const int d = frag_col<kFp8, D>(n, e, ln);
+    if (whole) {
+      const int h = (j / p.NHC) * p.G + hc * p.R + row;
+      store_out<QBF16>(p.out, (static_cast<size_t>(bq) * p.Hq + h) * D + d,
+                       acc * o_mult);
+    } else {
+      p.part_o[(static_cast<size_t>(slot) * C::kRowsPad + row) * D + d] = acc;
+    }
+  }
+  if (!whole)
+    for (int row = t; row < HB * 16; row += kNT)
+      p.part_lse[static_cast<size_t>(slot) * C::kRowsPad + row] =
+          s_rowlse[row];
+  ptx::named_bar_sync(kBar, kNT);
+}
+
+// Split combine of unit u (covered by blocks cf..cl): the output rows from
+// all partials, one pass with a running maximum, the loads of kB partials x
+// kE elements per thread in flight together.  Run by kNT threads.
+template <int KV, bool QBF16, int D, int HB, int kNT, int kE>
+__device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
+                                             int u, int b, int j, int cf,
+                                             int cl) {
+  using C = Cfg<KV, D, HB>;
+  constexpr bool kFp8 = (KV == kKvE4M3);
+  constexpr int kB = 4;
+  const int kvh = j / p.NHC, hc = j % p.NHC;
+  const float om = kFp8 ? __ldg(p.v_scale + b * p.Hkv + kvh) : 1.f;
+  // valid rows of this head chunk, row-major elements (row, d)
+  const int nv = min(p.R, p.G - hc * p.R) * D;
+  const size_t h_base =
+      (static_cast<size_t>(b) * p.Hq + kvh * p.G + hc * p.R) * D;
+  for (int v0 = t; v0 < nv; v0 += kE * kNT) {
+    float M[kE], lt[kE], acc[kE];
+#pragma unroll
+    for (int x = 0; x < kE; ++x) {
+      M[x] = -INFINITY;
+      lt[x] = 0.f;
+      acc[x] = 0.f;
+    }
+    for (int c0 = cf; c0 <= cl; c0 += kB) {
+      float ls[kB][kE], ov[kB][kE];
+#pragma unroll
+      for (int k = 0; k < kB; ++k)
+#pragma unroll
+        for (int x = 0; x < kE; ++x) {
+          const int v = v0 + x * kNT;
+          const bool ok = c0 + k <= cl && v < nv;
+          const size_t sl = static_cast<size_t>(c0 + k + u);
+          ls[k][x] =
+              ok ? __ldcg(p.part_lse + sl * C::kRowsPad + v / D) : -INFINITY;
+          ov[k][x] = ok ? __ldcg(p.part_o + sl * C::kRowsPad * D + v) : 0.f;
+        }
+#pragma unroll
+      for (int x = 0; x < kE; ++x) {
+        const float Mn = fmaxf(
+            M[x], fmaxf(fmaxf(ls[0][x], ls[1][x]), fmaxf(ls[2][x], ls[3][x])));
+        if (Mn == -INFINITY) continue;
+        const float a = ptx::ex2(M[x] - Mn);  // 0 while M is -inf
+        lt[x] *= a;
+        acc[x] *= a;
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+          const float f = ptx::ex2(ls[k][x] - Mn);
+          lt[x] += f;
+          acc[x] += f * ov[k][x];
+        }
+        M[x] = Mn;
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < kE; ++x) {
+      const int v = v0 + x * kNT;
+      if (v < nv)
+        store_out<QBF16>(p.out, h_base + v,
+                         (lt[x] > 0.f ? acc[x] / lt[x] : 0.f) * om);
+    }
+  }
+  if (t == 0) p.counters[u] = 0u;
+}
+
 template <int KV, bool QBF16, int D, int HB>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap map_k,
@@ -345,43 +509,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kFp8 = (KV == kKvE4M3);
   constexpr bool kMmaBF16 = !kFp8 && QBF16;
   using QT = typename std::conditional<QBF16, __nv_bfloat16, __half>::type;
+  constexpr int kPos = C::kOTiles * 4 * 32;  // fragment positions per warp
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  float* mrg_o = reinterpret_cast<float*>(ring + C::kRingBytes);
-  float* mrg_m = mrg_o + kConsumerWarps * 16 * D;
-  float* mrg_l = mrg_m + kConsumerWarps * 16;
-  uint64_t* full = reinterpret_cast<uint64_t*>(mrg_l + kConsumerWarps * 16);
+  // Dump area of the unit epilogue: per consumer warp its O fragments
+  // (position (n*4 + e)*32 + lane), row maxima and row sums.
+  float* dmp_o = reinterpret_cast<float*>(ring + C::kRingBytes);
+  float* dmp_m = dmp_o + kConsumerWarps * 16 * D;
+  float* dmp_l = dmp_m + kConsumerWarps * 16;
+  uint64_t* full = reinterpret_cast<uint64_t*>(dmp_l + kConsumerWarps * 16);
   uint64_t* empty = full + C::kStages;
+  uint64_t* dump_full = empty + C::kStages;   // 8 consumer warps arrive
+  uint64_t* dump_empty = dump_full + 1;       // the merge warps arrive
   __shared__ long long s_red[kThreads / 32];
   __shared__ long long s_pref0;
   __shared__ int s_b0;
   __shared__ int s_found;
   __shared__ volatile int s_abort;
   __shared__ float s_rowlse[HB * 16];   // log2-sum-exp per merged row
+  // descriptor of the unit whose states are in the dump area; s_dstop marks
+  // the block's last unit, which the consumers merge themselves
+  __shared__ int s_du, s_db, s_dj, s_dcf, s_dcl, s_dstop;
   // Units this block covers only in part (at most the first and the last of
-  // its range); their split combine runs after the main loop.
+  // its range), with the block's arrival ticket; their split combine runs
+  // after the block's last unit.
+  __shared__ int s_npend;
   __shared__ int s_pend_u[2], s_pend_b[2], s_pend_j[2], s_pend_cf[2],
       s_pend_cl[2], s_pend_last[2];
+  __shared__ uint32_t s_pend_t[2];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
   const int HU = p.Hkv * p.NHC;  // units per sequence
 
+  if (warp == 0 && lane == 0) {
+    // descriptor fetch overlaps the scheduler prologue
+    ptx::prefetch_tensormap(&map_k);
+    ptx::prefetch_tensormap(&map_v);
+  }
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], kGroupWarps);
     }
+    ptx::mbar_init(dump_full, kConsumerWarps);
+    ptx::mbar_init(dump_empty, 1);
     ptx::fence_barrier_init();
     s_abort = 0;
+    s_npend = 0;
     s_found = 0;
     s_b0 = 0;
     s_pref0 = 0;
   }
+  // Launched as a programmatic dependent of the previous kernel in the
+  // stream: everything above overlapped its tail; nothing before this point
+  // reads global memory (q, the caches and seq_lens may be written by it).
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   // ---- flat tile list: total N, this block's range, its first sequence ----
   // Blocks that take part: at most one per tile (P = min(grid, N)), so that
@@ -452,11 +640,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     w0.ti = static_cast<int>(off % w0.nt);
   }
 
-  if (warp == kConsumerWarps) {
+  if (warp < 4) {
+    ptx::setmaxnreg_dec<kRegsSmall>();
+  } else {
+    ptx::setmaxnreg_inc<kRegsBig>();
+  }
+
+  if (warp == 0) {
     // =============================== producer ===============================
     if (lane == 0 && t0 < t1) {
-      ptx::prefetch_tensormap(&map_k);
-      ptx::prefetch_tensormap(&map_v);
       const uint64_t policy = ptx::policy_evict_first();
       TileWalk w = w0;
       long long it = 0;
@@ -497,22 +689,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // ================================ consumers ===============================
-  const int cw = warp;                       // consumer warp 0..7
-  const int ct = tid;                        // consumer thread 0..255
+  if (warp < 4) {
+    // ================================= merge =================================
+    const int mt = tid - 32;  // 0 .. kMergeThreads-1
+    // Sequences with no valid token: all-zero output rows.
+    for (int b = cta; b < p.B; b += gridDim.x) {
+      if (clamp_len(__ldg(p.seq_lens + b), p.Smax) != 0) continue;
+      const size_t base = static_cast<size_t>(b) * p.Hq * D;
+      for (int i = mt; i < p.Hq * D; i += kMergeThreads)
+        store_out<QBF16>(p.out, base + i, 0.f);
+    }
+    if (t0 >= t1) return;
+
+    // Units that end inside this block's range, in order; the block's last
+    // unit is merged by the consumers themselves (descriptor s_dstop).
+    uint32_t kph = 0;  // parity of the dump being waited for
+    while (true) {
+      if (!ptx::mbar_wait_bounded(dump_full, kph, kWaitLimitNs)) {
+        atomicOr(p.error, kErrWaitTimeout);
+        s_abort = 1;
+        return;
+      }
+      kph ^= 1u;
+      if (s_dstop) return;
+      const int u = s_du, bq = s_db, j = s_dj;
+      const int c_first = s_dcf, c_last = s_dcl;
+      const bool whole = (c_first == c_last);
+      merge_unit<KV, QBF16, D, HB, kMergeThreads, 2>(
+          mt, dmp_o, dmp_m, dmp_l, s_rowlse, p, u, bq, j, whole, cta);
+      // A partial also counts this block's arrival (acquire-release add: the
+      // merge warps' partial stores are ordered before it by their barrier);
+      // the ticket is kept for the combine after the block's last unit.
+      if (mt == 0) {
+        if (!whole && s_npend < 2) {
+          const int k = s_npend;
+          s_pend_t[k] = ptx::atom_add_acq_rel_gpu(p.counters + u, 1u);
+          s_pend_u[k] = u;
+          s_pend_b[k] = bq;
+          s_pend_j[k] = j;
+          s_pend_cf[k] = c_first;
+          s_pend_cl[k] = c_last;
+          s_npend = k + 1;
+        }
+        ptx::mbar_arrive(dump_empty);  // the dump area is free again
+      }
+    }
+  }
+
+  // =============================== consumers ================================
+  const int cw = warp - kFirstConsumerWarp;  // consumer warp 0..7
   const int grp = cw / kGroupWarps;          // ping-pong group
   const int lw = cw % kGroupWarps;           // warp within the group
   const int hb = lw / C::kWarpsPerBlock;     // head block of this warp
   const int wsl = lw % C::kWarpsPerBlock;    // token slice of this warp
   const int r = lane >> 2, cq = lane & 3;    // mma fragment coordinates
-
-  // Sequences with no valid token: all-zero output rows.
-  for (int b = cta; b < p.B; b += gridDim.x) {
-    if (clamp_len(__ldg(p.seq_lens + b), p.Smax) != 0) continue;
-    const size_t base = static_cast<size_t>(b) * p.Hq * D;
-    for (int i = ct; i < p.Hq * D; i += kConsumerThreads)
-      store_out<QBF16>(p.out, base + i, 0.f);
-  }
   if (t0 >= t1) return;
 
   TileWalk w = w0;
@@ -522,10 +752,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float s_mult = 0.f, o_mult = 1.f;
   bool fresh = true;
   bool aborted = false;  // this warp gave up on a wait: skip further waits
-  // ticket of this block's arrival on a partly covered unit (thread 0 only)
-  uint32_t ticket0 = 0u, ticket1 = 0u;
-  int n_pend = 0;  // partly covered units met so far (at most 2)
-  if (ct == 0) s_pend_u[0] = s_pend_u[1] = -1;
 
   // This thread's two fragment rows within its head block, and their query
   // rows for unit (kvh, hc) of sequence b.
@@ -542,9 +768,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   issue_q(w.b, w.j / p.NHC, w.j % p.NHC);
 
-  long long it = 0;
-  for (long long g = t0; g < t1; ++g, ++it) {
-    const int kvh = w.j / p.NHC, hc = w.j % p.NHC;
+  int stage = 0;     // ring stage of tile g: (g - t0) % kStages
+  uint32_t ph = 0;   // its phase parity: ((g - t0) / kStages) & 1
+  int par = 0;       // (g - t0) & 1: the group that computes tile g
+  uint32_t dph = 0;  // parity of this block's unit epilogues so far
+  for (long long g = t0; g < t1; ++g) {
+    const int kvh = w.j / p.NHC;
     if (fresh) {
       // ---- new unit: softmax state and multipliers (q already issued) ----
       fresh = false;
@@ -564,10 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       l[0] = l[1] = 0.f;
     }
 
-    if ((it & 1) == grp) {
+    if (par == grp) {
     // ---- wait for the stage (tiles alternate between the two groups) ----
-    const int stage = static_cast<int>(it % C::kStages);
-    const uint32_t ph = static_cast<uint32_t>((it / C::kStages) & 1);
     if (!aborted && !ptx::mbar_wait_bounded(&full[stage], ph, kWaitLimitNs)) {
       atomicOr(p.error, kErrWaitTimeout);
       aborted = true;
@@ -789,30 +1016,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const bool unit_end = (w.ti == w.nt - 1) || (g == t1 - 1);
     if (unit_end) {
-      // ================= unit (segment) epilogue =================
-      const int u = w.b * HU + w.j;
-      const long long us = w.pref + static_cast<long long>(w.j) * w.nt;
-      const int c_first = block_of_tile(us, N, P);
-      const int c_last = block_of_tile(us + w.nt - 1, N, P);
-      const bool whole = (c_first == c_last);
-      const int bq = w.b;
-      // The next unit's query rows load while this epilogue runs (qf is dead
-      // after the unit's last QK^T).
-      if (g + 1 < t1) {
-        TileWalk wn = w;
-        wn.next(p, HU);
-        issue_q(wn.b, wn.j / p.NHC, wn.j % p.NHC);
+      // ============ unit epilogue: hand the state to the merge warps ========
+      // wait until the merge warps have finished with the previous dump
+      if (!aborted &&
+          !ptx::mbar_wait_bounded(dump_empty, dph ^ 1u, kWaitLimitNs)) {
+        atomicOr(p.error, kErrWaitTimeout);
+        aborted = true;
+        s_abort = 1;
       }
-
-      // 1) this warp's state -> shared memory in mma fragment order
-      //    (position (n*4 + e)*32 + lane: conflict-free), valid rows only
+      dph ^= 1u;
       float lt0 = l[0], lt1 = l[1];
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 1);
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 1);
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
       const bool hi_rows = hb * 16 + 8 < p.R;  // rows r+8 exist (uniform)
-      float* mo = mrg_o + cw * 16 * D;
+      float* mo = dmp_o + cw * 16 * D;
 #pragma unroll
       for (int n = 0; n < C::kOTiles; ++n) {
         mo[(n * 4 + 0) * 32 + lane] = o[n][0];
@@ -823,170 +1042,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (cq == 0) {
-        mrg_m[cw * 16 + r] = m[0];
-        mrg_m[cw * 16 + r + 8] = m[1];
-        mrg_l[cw * 16 + r] = lt0;
-        mrg_l[cw * 16 + r + 8] = lt1;
+        dmp_m[cw * 16 + r] = m[0];
+        dmp_m[cw * 16 + r + 8] = m[1];
+        dmp_l[cw * 16 + r] = lt0;
+        dmp_l[cw * 16 + r + 8] = lt1;
       }
-      ptx::named_bar_sync(1, kConsumerThreads);
-
-      // 2) per merged row: the max over warps, the total, and each warp's
-      //    weight exp2(m_w - M) / total (written over m_w)
-      if (ct < HB * 16) {
-        const int hbk = ct >> 4, rr = ct & 15;
-        float M = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
-          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
-                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
-          M = fmaxf(M, mrg_m[wk * 16 + rr]);
-        }
-        const float Mb = (M == -INFINITY) ? 0.f : M;
-        float lt = 0.f;
-        float f[kGroups * C::kWarpsPerBlock];
-#pragma unroll
-        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
-          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
-                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
-          f[k] = ptx::ex2(mrg_m[wk * 16 + rr] - Mb);
-          lt += mrg_l[wk * 16 + rr] * f[k];
-        }
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll
-        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
-          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
-                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
-          mrg_m[wk * 16 + rr] = f[k] * inv;
-        }
-        s_rowlse[ct] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
+      const bool last = (g == t1 - 1);
+      const long long us = w.pref + static_cast<long long>(w.j) * w.nt;
+      const int u = w.b * HU + w.j;
+      const int c_first = block_of_tile(us, N, P);
+      const int c_last = block_of_tile(us + w.nt - 1, N, P);
+      if (cw == 0 && lane == 0) {
+        s_du = u;
+        s_db = w.b;
+        s_dj = w.j;
+        s_dcf = c_first;
+        s_dcl = c_last;
+        s_dstop = last ? 1 : 0;
       }
-      ptx::named_bar_sync(1, kConsumerThreads);
-
-      // 3) merge position by position; write the output rows (unit covered by
-      //    this block alone) or the normalised partial ([row][d], fp32)
-      const int slot = whole ? 0 : cta + u;
-      constexpr int kPos = C::kOTiles * 4 * 32;  // positions per head block
-      for (int idx = ct; idx < HB * kPos; idx += kConsumerThreads) {
-        const int hbk = idx / kPos, pos = idx % kPos;
-        const int n = pos >> 7, e = (pos >> 5) & 3, ln = pos & 31;
-        const int rr = (ln >> 2) + 8 * (e >> 1);
-        const int row = hbk * 16 + rr;
-        if (row >= p.R || hc * p.R + row >= p.G) continue;  // warp-uniform
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < kGroups * C::kWarpsPerBlock; ++k) {
-          const int wk = (k / C::kWarpsPerBlock) * kGroupWarps +
-                         hbk * C::kWarpsPerBlock + k % C::kWarpsPerBlock;
-          acc += mrg_m[wk * 16 + rr] * mrg_o[wk * 16 * D + pos];
-        }
-        if (whole) {
-          const int h = kvh * p.G + hc * p.R + row;
-          store_out<QBF16>(p.out,
-                           (static_cast<size_t>(bq) * p.Hq + h) * D +
-                               frag_col<kFp8, D>(n, e, ln),
-                           acc * o_mult);
-        } else {
-          p.part_o[(static_cast<size_t>(slot) * C::kRowsPad + row) * D +
-                   frag_col<kFp8, D>(n, e, ln)] = acc;
-        }
-      }
-      if (!whole && ct < HB * 16)
-        p.part_lse[static_cast<size_t>(slot) * C::kRowsPad + ct] = s_rowlse[ct];
-      ptx::named_bar_sync(1, kConsumerThreads);
-
-      // 4) partial: count this block's arrival (release: all the block's
-      //    partial stores are ordered before it by the barrier and the
-      //    fence); whether this block is the unit's last arrival is only
-      //    looked at after the main loop
-      if (!whole && n_pend < 2) {
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(dump_full);
+      if (!last) {
+        // the next unit's query rows load while the merge warps work
+        TileWalk wn = w;
+        wn.next(p, HU);
+        issue_q(wn.b, wn.j / p.NHC, wn.j % p.NHC);
+        fresh = true;
+      } else {
+        // ---- the block's last unit: all consumer threads merge it ----
+        const int ct = tid - kFirstConsumerWarp * 32;  // 0 .. 255
+        ptx::named_bar_sync(1, kConsumerThreads);  // every warp's dump
+        const bool whole = (c_first == c_last);
+        merge_unit<KV, QBF16, D, HB, kConsumerThreads, 1>(
+            ct, dmp_o, dmp_m, dmp_l, s_rowlse, p, u, w.b, w.j, whole, cta);
         if (ct == 0) {
-          __threadfence();
-          const uint32_t t = atomicAdd(p.counters + u, 1u);
-          if (n_pend == 0) ticket0 = t; else ticket1 = t;
-          s_pend_u[n_pend] = u;
-          s_pend_b[n_pend] = bq;
-          s_pend_j[n_pend] = w.j;
-          s_pend_cf[n_pend] = c_first;
-          s_pend_cl[n_pend] = c_last;
+          if (!whole && s_npend < 2) {
+            const int k = s_npend;
+            s_pend_t[k] = ptx::atom_add_acq_rel_gpu(p.counters + u, 1u);
+            s_pend_u[k] = u;
+            s_pend_b[k] = w.b;
+            s_pend_j[k] = w.j;
+            s_pend_cf[k] = c_first;
+            s_pend_cl[k] = c_last;
+            s_npend = k + 1;
+          }
+          // last arrival of a unit: this block combines its partials
+          // (the acquire side of both adds: what the other blocks released
+          // before their arrivals is visible to this thread, and to the
+          // others through the barrier below)
+          for (int i = 0; i < 2; ++i)
+            s_pend_last[i] =
+                i < s_npend && s_pend_t[i] == static_cast<uint32_t>(
+                                                  s_pend_cl[i] - s_pend_cf[i]);
         }
-        ++n_pend;
+        ptx::named_bar_sync(1, kConsumerThreads);
+        for (int i = 0; i < 2; ++i)
+          if (s_pend_last[i])  // uniform
+            combine_unit<KV, QBF16, D, HB, kConsumerThreads, 4>(
+                ct, p, s_pend_u[i], s_pend_b[i], s_pend_j[i], s_pend_cf[i],
+                s_pend_cl[i]);
       }
-      fresh = true;
+    }
+    par ^= 1;
+    if (++stage == C::kStages) {
+      stage = 0;
+      ph ^= 1u;
     }
     w.next(p, HU);
-  }
-
-  // ---- split combine of the units whose last arrival was this block ----
-  if (ct == 0) {
-    s_pend_last[0] = n_pend > 0 &&
-        ticket0 == static_cast<uint32_t>(s_pend_cl[0] - s_pend_cf[0]);
-    s_pend_last[1] = n_pend > 1 &&
-        ticket1 == static_cast<uint32_t>(s_pend_cl[1] - s_pend_cf[1]);
-    __threadfence();  // acquire: other blocks' partials before the reads below
-  }
-  ptx::named_bar_sync(1, kConsumerThreads);
-  for (int i = 0; i < 2; ++i) {
-    if (!s_pend_last[i]) continue;  // uniform
-    const int u = s_pend_u[i], b = s_pend_b[i], j = s_pend_j[i];
-    const int kvh = j / p.NHC, hc = j % p.NHC;
-    const int cf = s_pend_cf[i], cl = s_pend_cl[i];
-    const float om = kFp8 ? __ldg(p.v_scale + b * p.Hkv + kvh) : 1.f;
-    // valid rows of this head chunk, row-major elements (row, d)
-    const int rows = min(p.R, p.G - hc * p.R);
-    const int nv = rows * D;
-    const size_t h_base =
-        (static_cast<size_t>(b) * p.Hq + kvh * p.G + hc * p.R) * D;
-    // Four elements per thread at a time, four partials per batch, all
-    // loads in flight together; running maximum across batches.
-    constexpr int kE = 4, kB = 4;
-    for (int v0 = ct; v0 < nv; v0 += kE * kConsumerThreads) {
-      float M[kE], lt[kE], acc[kE];
-#pragma unroll
-      for (int x = 0; x < kE; ++x) {
-        M[x] = -INFINITY;
-        lt[x] = 0.f;
-        acc[x] = 0.f;
-      }
-      for (int c0 = cf; c0 <= cl; c0 += kB) {
-        float ls[kB][kE], ov[kB][kE];
-#pragma unroll
-        for (int k = 0; k < kB; ++k)
-#pragma unroll
-          for (int x = 0; x < kE; ++x) {
-            const int v = v0 + x * kConsumerThreads;
-            const bool ok = c0 + k <= cl && v < nv;
-            const size_t sl = static_cast<size_t>(c0 + k + u);
-            ls[k][x] = ok ? __ldcg(p.part_lse + sl * C::kRowsPad + v / D)
-                          : -INFINITY;
-            ov[k][x] = ok ? __ldcg(p.part_o + sl * C::kRowsPad * D + v) : 0.f;
-          }
-#pragma unroll
-        for (int x = 0; x < kE; ++x) {
-          const float Mn =
-              fmaxf(M[x], fmaxf(fmaxf(ls[0][x], ls[1][x]),
-                                fmaxf(ls[2][x], ls[3][x])));
-          if (Mn == -INFINITY) continue;
-          const float a = ptx::ex2(M[x] - Mn);  // 0 while M is -inf
-          lt[x] *= a;
-          acc[x] *= a;
-#pragma unroll
-          for (int k = 0; k < kB; ++k) {
-            const float f = ptx::ex2(ls[k][x] - Mn);
-            lt[x] += f;
-            acc[x] += f * ov[k][x];
-          }
-          M[x] = Mn;
-        }
-      }
-#pragma unroll
-      for (int x = 0; x < kE; ++x) {
-        const int v = v0 + x * kConsumerThreads;
-        if (v < nv)
-          store_out<QBF16>(p.out, h_base + v,
-                           (lt[x] > 0.f ? acc[x] / lt[x] : 0.f) * om);
-      }
-    }
-    if (ct == 0) p.counters[u] = 0u;
   }
 }
 

@@ -203,6 +203,55 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (no-op without such a
+// dependency); allow the next grid in the stream to start launching.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Global atomic add with release semantics at GPU scope (orders the calling
+// thread's prior writes, and those ordered before it by a CTA barrier,
+// before the add).
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* addr,
+                                                         uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
+// The same with acquire-release semantics: additionally, what other threads
+// released before their adds is visible to the caller afterwards.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* addr,
+                                                         uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Warpgroup register reallocation: every warp of a warpgroup executes the
+// same instruction; .dec returns registers to the block's pool, .inc waits
+// for them.
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs) : "memory");
+}
+
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -59,6 +59,8 @@ CASES = [
      ("ragged", 0, 70)),
     ("fp8_many_sequences", 290, 8, 2, 128, 80, "bf16", "e4m3",
      ("ragged", 0, 80)),
+    ("bf16_more_sequences_than_threads", 400, 8, 2, 64, 60, "bf16", "same",
+     ("ragged", 0, 60)),
 ]
 
 
