@@ -382,52 +382,71 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
   };
 
   // 1) per merged row: the max over the head block's warps, the total, and
-  //    each warp's weight exp2(m_w - M) / total (written over m_w)
-  for (int row = t; row < HB * 16; row += kNT) {
+  //    each warp's weight exp2(m_w - M) / total (written over m_w).  One
+  //    thread per (row, warp); the kW threads of a row are adjacent lanes and
+  //    reduce with shuffles.
+  static_assert(32 % kW == 0, "a row's warps must share a warp of threads");
+  for (int i = t; i < HB * 16 * kW; i += kNT) {  // warp-uniform bounds
+    const int row = i / kW, k = i % kW;
     const int hbk = row >> 4, rr = row & 15;
-    float M = -INFINITY;
+    const int wk = warp_of(hbk, k);
+    const float mv = dmp_m[wk * 16 + rr], lv = dmp_l[wk * 16 + rr];
+    float M = mv;
 #pragma unroll
-    for (int k = 0; k < kW; ++k) M = fmaxf(M, dmp_m[warp_of(hbk, k) * 16 + rr]);
+    for (int o = 1; o < kW; o <<= 1)
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mb = (M == -INFINITY) ? 0.f : M;
-    float lt = 0.f;
-    float f[kW];
+    const float f = ptx::ex2(mv - Mb);
+    float lt = lv * f;
 #pragma unroll
-    for (int k = 0; k < kW; ++k) {
-      const int wk = warp_of(hbk, k);
-      f[k] = ptx::ex2(dmp_m[wk * 16 + rr] - Mb);
-      lt += dmp_l[wk * 16 + rr] * f[k];
-    }
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll
-    for (int k = 0; k < kW; ++k) dmp_m[warp_of(hbk, k) * 16 + rr] = f[k] * inv;
-    s_rowlse[row] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
+    for (int o = 1; o < kW; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+    dmp_m[wk * 16 + rr] = lt > 0.f ? f / lt : 0.f;
+    if (k == 0) s_rowlse[row] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
   }
   ptx::named_bar_sync(kBar, kNT);
 
-  // 2) merge position by position (positions of one warp-sized run share
-  //    (n, e), so the row test below is uniform across a warp)
+  // 2) merge position by position.  A fragment slot (head block, element e,
+  //    lane) is one row; a thread keeps its slot while it walks the n-tiles,
+  //    so the row's weights are loaded once.  When no head block has more
+  //    than 8 rows, slots e = 2, 3 (rows 8..15) are never visited.
   const int slot = whole ? 0 : cta + u;
-  for (int idx = t; idx < HB * kPos; idx += kNT) {
-    const int hbk = idx / kPos, pos = idx % kPos;
-    const int n = pos >> 7, e = (pos >> 5) & 3, ln = pos & 31;
-    const int rr = (ln >> 2) + 8 * (e >> 1);
-    const int row = hbk * 16 + rr;
-    if (row >= p.R || hc * p.R + row >= p.G) continue;
-    float acc = 0.f;
+  const int hq0 = (j / p.NHC) * p.G + hc * p.R;  // first query head of unit
+  auto merge_slots = [&](auto e_count) {
+    constexpr int kEs = decltype(e_count)::value;  // elements e in use
+    constexpr int kSlotCount = HB * kEs * 32;
+    float wt[kW];
+    int wrow = -1;
+    for (int wi = t; wi < kSlotCount * C::kOTiles; wi += kNT) {
+      const int sl = wi % kSlotCount, n = wi / kSlotCount;
+      const int hbk = sl / (kEs * 32), e = (sl / 32) % kEs, ln = sl & 31;
+      const int rr = (ln >> 2) + 8 * (e >> 1);
+      const int row = hbk * 16 + rr;
+      if (row >= p.R || hc * p.R + row >= p.G) continue;
+      if (row != wrow) {
+        wrow = row;
 #pragma unroll
-    for (int k = 0; k < kW; ++k) {
-      const int wk = warp_of(hbk, k);
-      acc += dmp_m[wk * 16 + rr] * dmp_o[wk * 16 * D + pos];
+        for (int k = 0; k < kW; ++k) wt[k] = dmp_m[warp_of(hbk, k) * 16 + rr];
+      }
+      const int pos = (n * 4 + e) * 32 + ln;
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < kW; ++k)
+        acc += wt[k] * dmp_o[warp_of(hbk, k) * 16 * D + pos];
+      const int d = frag_col<kFp8, D>(n, e, ln);
+      if (whole) {
+        store_out<QBF16>(
+            p.out, (static_cast<size_t>(bq) * p.Hq + hq0 + row) * D + d,
+            acc * o_mult);
+      } else {
+        p.part_o[(static_cast<size_t>(slot) * C::kRowsPad + row) * D + d] =
+            acc;
+      }
     }
-    const int d = frag_col<kFp8, D>(n, e, ln);
-    if (whole) {
-      const int h = (j / p.NHC) * p.G + hc * p.R + row;
-      store_out<QBF16>(p.out, (static_cast<size_t>(bq) * p.Hq + h) * D + d,
-                       acc * o_mult);
-    } else {
-      p.part_o[(static_cast<size_t>(slot) * C::kRowsPad + row) * D + d] = acc;
-    }
-  }
+  };
+  if (HB == 1 && p.R <= 8)
+    merge_slots(std::integral_constant<int, 2>{});
+  else
+    merge_slots(std::integral_constant<int, 4>{});
   if (!whole)
     for (int row = t; row < HB * 16; row += kNT)
       p.part_lse[static_cast<size_t>(slot) * C::kRowsPad + row] =
