@@ -219,7 +219,7 @@ def main(argv=None):
            "D": w.D, "seq_len": (w.Smax if w.lens[0] == "uniform" else
                                  f"uniform[{w.lens[1]},{w.lens[2]}]"),
            "Smax": w.Smax, "qo_dtype": w.dtype,
-           "kv_dtype": "e4m3" if w.kv == "e4m3" else w.dtype,
+           "kv_dtype": w.kv if w.kv != "same" else w.dtype,
            "l2": "inputs larger than L2, K/V loaded evict-first; no flush",
            "parallelism": "replicas" if a.gpus > 1 else "single"}
     warmup = max(3, a.warmup)
@@ -363,8 +363,8 @@ def main(argv=None):
         "metric": METRIC, "value": job_us_per_step, "unit": "us/step",
         "n_gpus": ws, "steps": K, "warmup": warmup,
         "ms_per_step": job_us_per_step / 1e3, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
-        w.kv != "e4m3" else "e4m3 KV / bf16 q,out", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if
+        w.kv == "same" else f"{w.kv} KV / {w.dtype} q,out", "data": "synthetic",
         "config": cfg,
         "kv_gbs": achieved * ws, "hbm_frac_of_" + peak_kind: achieved / peak,
         "hbm_frac_of_spec_8tbs": achieved / SPEC_HBM_GBS,

@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(PKG, "libgqa_b300.so")
 
 GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, \
     GQA_ERR_DEVICE = 0, 1, 2, 3, 4
-GQA_F16, GQA_BF16, GQA_E4M3 = 0, 1, 2
+GQA_F16, GQA_BF16, GQA_E4M3, GQA_E5M2 = 0, 1, 2, 3
 
 # Every function include/gqa.h declares, with its ctypes signature.
 _VP, _I32, _F32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -36,7 +36,7 @@ SIGNATURES = {
     "gqa_decode": (_I32, [_VP, _VP, _VP, _VP, _F32, _VP, _I32, _I32, _I32,
                           _I32, _I32, _I32, _VP]),
     "gqa_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
-                              _I32, _I32, _I32, _I32, _I32, _VP]),
+                              _I32, _I32, _I32, _I32, _I32, _I32, _VP]),
     "gqa_decode_static": (_I32, [_VP, _VP, _VP, _VP, _F32, _VP, _I32, _I32,
                                  _I32, _I32, _I32, _I32, _VP]),
     "gqa_kv_bytes_per_token": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
@@ -119,6 +119,18 @@ def _dtype_code(t) -> int:
     raise TypeError(f"q/out must be float16 or bfloat16, got {t.dtype}")
 
 
+def _fp8_code(t) -> int:
+    """GQA_E4M3 / GQA_E5M2 for an 8-bit cache tensor (uint8 codes are read as
+    E4M3)."""
+    import torch
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return GQA_E4M3
+    if t.dtype == torch.float8_e5m2:
+        return GQA_E5M2
+    raise TypeError(f"8-bit cache must be float8_e4m3fn or float8_e5m2, "
+                    f"got {t.dtype}")
+
+
 def _check_dev(name, t):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -187,9 +199,10 @@ def gqa_decode_static(q, k_cache, v_cache, seq_lens, scale: float, out=None,
 
 def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens,
                    scale: float, out=None, stream=None):
-    """GQA decode step over an FP8 E4M3 cache; returns ``out`` [B, Hq, D].
+    """GQA decode step over an 8-bit cache; returns ``out`` [B, Hq, D].
 
-    k_cache / v_cache [B, Hkv, Smax, D] float8_e4m3fn (or uint8 codes),
+    k_cache / v_cache [B, Hkv, Smax, D] float8_e4m3fn (or uint8 E4M3 codes)
+    or float8_e5m2,
     k_scale / v_scale [B, Hkv] float32; other arguments as gqa_decode.
     """
     import torch
@@ -197,9 +210,9 @@ def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens,
                  ("k_scale", k_scale), ("v_scale", v_scale),
                  ("seq_lens", seq_lens)):
         _check_dev(n, t)
-    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
-        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
-            raise TypeError(f"{n} must be float8_e4m3fn, got {t.dtype}")
+    kv_code = _fp8_code(k_cache)
+    if _fp8_code(v_cache) != kv_code:
+        raise TypeError("k_cache and v_cache must share a dtype")
     if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
         raise TypeError("k_scale / v_scale must be float32")
     if seq_lens.dtype != torch.int32:
@@ -213,7 +226,8 @@ def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens,
                               v_cache.data_ptr(), k_scale.data_ptr(),
                               v_scale.data_ptr(), seq_lens.data_ptr(),
                               float(scale), out.data_ptr(), B, Hq, Hkv, Smax,
-                              D, _dtype_code(q), _stream_handle(stream))
+                              D, kv_code, _dtype_code(q),
+                              _stream_handle(stream))
     if st != GQA_OK:
         raise GQAError(st, "gqa_decode_fp8")
     return out
@@ -249,8 +263,8 @@ class BoundDecode:
             self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),
                           inp["k_scale"].data_ptr(), inp["v_scale"].data_ptr(),
                           inp["seq_lens"].data_ptr(), float(inp["scale"]),
-                          out.data_ptr(), B, Hq, Hkv, Smax, D, _dtype_code(q),
-                          h)
+                          out.data_ptr(), B, Hq, Hkv, Smax, D, _fp8_code(k),
+                          _dtype_code(q), h)
         else:
             self._fn = lib().gqa_decode
             self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <utility>
 
@@ -59,6 +60,34 @@ bool make_cache_map(CUtensorMap* map, const void* base, int elem_bytes,
   return r == CUDA_SUCCESS;
 }
 
+// Encoded descriptors of recently used caches: a descriptor only records the
+// base address, shape and strides, so it stays valid for any later call on
+// the same (pointer, shape).  Bounded; cleared when full.  Guarded by g_mu.
+struct MapKey {
+  const void* base;
+  int elem_bytes, B, Hkv, Smax, D;
+  bool operator<(const MapKey& o) const {
+    return std::tie(base, elem_bytes, B, Hkv, Smax, D) <
+           std::tie(o.base, o.elem_bytes, o.B, o.Hkv, o.Smax, o.D);
+  }
+};
+std::map<MapKey, CUtensorMap> g_maps;
+constexpr size_t kMaxCachedMaps = 256;
+
+bool cached_cache_map(CUtensorMap* map, const void* base, int elem_bytes,
+                      int B, int Hkv, int Smax, int D) {
+  const MapKey key{base, elem_bytes, B, Hkv, Smax, D};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *map = it->second;
+    return true;
+  }
+  if (!make_cache_map(map, base, elem_bytes, B, Hkv, Smax, D)) return false;
+  if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+  g_maps.emplace(key, *map);
+  return true;
+}
+
 // ----------------------------------------------------------- kernel table
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap,
@@ -91,6 +120,8 @@ Variant pick_d(int D, int hb) {
 Variant pick(int kv, bool q_bf16, int D, int hb) {
   if (kv == kKvF16) return pick_d<kKvF16, false>(D, hb);
   if (kv == kKvBF16) return pick_d<kKvBF16, true>(D, hb);
+  if (kv == kKvE5M2)
+    return q_bf16 ? pick_d<kKvE5M2, true>(D, hb) : pick_d<kKvE5M2, false>(D, hb);
   return q_bf16 ? pick_d<kKvE4M3, true>(D, hb) : pick_d<kKvE4M3, false>(D, hb);
 }
 
@@ -230,14 +261,14 @@ gqa_status launch(const void* q, const void* k, const void* v,
   if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
 
   const Variant var = pick(kv_kind, q_bf16, D, hb);
-  const int elem_bytes = kv_kind == kKvE4M3 ? 1 : 2;
-
-  CUtensorMap map_k, map_v;
-  if (!make_cache_map(&map_k, k, elem_bytes, B, Hkv, Smax, D) ||
-      !make_cache_map(&map_v, v, elem_bytes, B, Hkv, Smax, D))
-    return GQA_ERR_CUDA;
+  const int elem_bytes = is_fp8(kv_kind) ? 1 : 2;
 
   std::lock_guard<std::mutex> lock(g_mu);
+  CUtensorMap map_k, map_v;
+  if (!cached_cache_map(&map_k, k, elem_bytes, B, Hkv, Smax, D) ||
+      !cached_cache_map(&map_v, v, elem_bytes, B, Hkv, Smax, D))
+    return GQA_ERR_CUDA;
+
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   int sms = 0, per_sm = 0;
@@ -438,9 +469,11 @@ gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
                           const void* v_cache, const float* k_scale,
                           const float* v_scale, const int32_t* seq_lens,
                           float scale, void* out, int B, int Hq, int Hkv,
-                          int Smax, int D, gqa_dtype qo_dtype, void* stream) {
+                          int Smax, int D, gqa_dtype kv_dtype,
+                          gqa_dtype qo_dtype, void* stream) {
   gqa::t_last_launches = 0;
   if (qo_dtype != GQA_F16 && qo_dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (kv_dtype != GQA_E4M3 && kv_dtype != GQA_E5M2) return GQA_ERR_INVALID_ARG;
   if (!k_scale || !v_scale || !gqa::aligned(k_scale, 4) ||
       !gqa::aligned(v_scale, 4))
     return GQA_ERR_INVALID_ARG;
@@ -449,7 +482,8 @@ gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
   if (st != GQA_OK) return st;
   try {
     return gqa::launch(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale,
-                       out, B, Hq, Hkv, Smax, D, gqa::kKvE4M3,
+                       out, B, Hq, Hkv, Smax, D,
+                       kv_dtype == GQA_E5M2 ? gqa::kKvE5M2 : gqa::kKvE4M3,
                        qo_dtype == GQA_BF16, stream);
   } catch (...) {
     return GQA_ERR_CUDA;

@@ -40,8 +40,9 @@
 //    rows it has already started loading.  The merge warps combine the eight
 //    states, write the output rows or a split partial, and publish the
 //    block's arrival, off the consumers' critical path.
-//  * FP8 E4M3 cache.  Bytes are turned into exact f16 pairs in registers
-//    (cvt.rn.f16x2.e4m3x2); q is moved into f16 with a per-head-block power
+//  * FP8 cache (E4M3 or E5M2).  Bytes are turned into exact f16 pairs in
+//    registers (cvt.rn.f16x2.e4m3x2; an E5M2 byte is the upper byte of its
+//    f16); q is moved into f16 with a per-head-block power
 //    of two so no value can overflow; k_scale and the power of two fold into
 //    the score multiplier and v_scale into the output.
 //  * Split combine.  A unit covered by one block is written out directly;
@@ -89,7 +90,12 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
 // less 1 KB left for the kernel's static shared variables.
 constexpr int kSmemBudget = 232448 - 1024;
 
-enum KvKind : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
+enum KvKind : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2, kKvE5M2 = 3 };
+
+// 8-bit cache element kinds (E4M3, E5M2); the others are 16-bit.
+__host__ __device__ constexpr bool is_fp8(int kv) {
+  return kv == kKvE4M3 || kv == kKvE5M2;
+}
 
 enum ErrorBits : uint32_t { kErrWaitTimeout = 1u };
 
@@ -113,13 +119,13 @@ struct DecodeParams {
 
 template <int KV, int D, int HB>
 struct Cfg {
-  static constexpr int kElemBytes = (KV == kKvE4M3) ? 1 : 2;
+  static constexpr int kElemBytes = is_fp8(KV) ? 1 : 2;
   static constexpr int kRowBytes = D * kElemBytes;            // one token
   static constexpr int kTileBytes = kTileTokens * kRowBytes;  // K or V tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   // TMA box: 128-byte rows for 16-bit (D=128 needs two boxes), the whole row
   // for E4M3 (128 B at D=128 -> 128B swizzle, 64 B at D=64 -> 64B swizzle).
-  static constexpr int kBoxElems = (KV == kKvE4M3) ? D : 64;
+  static constexpr int kBoxElems = is_fp8(KV) ? D : 64;
   static constexpr int kBoxBytes = kTileTokens * kBoxElems * kElemBytes;
   static constexpr int kBoxesPerTile = D / kBoxElems;
   static constexpr int kWarpsPerBlock = kGroupWarps / HB;  // per head block
@@ -346,6 +352,27 @@ __device__ __forceinline__ int fp8_finish_q(uint32_t (&qf)[D / 16][4]) {
   return e;
 }
 
+// Two 8-bit cache elements (bytes 0 and 1, or bytes 2 and 3, of w) -> two
+// exact f16 values packed low/high.  E4M3: the hardware conversion.  E5M2 is
+// the upper byte of an IEEE binary16, so its f16 is the byte moved up.
+template <int KV>
+__device__ __forceinline__ uint32_t fp8_lo(uint32_t w) {
+  if constexpr (KV == kKvE5M2) {
+    return __byte_perm(w, 0u, 0x1404);
+  } else {
+    return ptx::e4m3x2_to_f16x2(w & 0xffffu);
+  }
+}
+
+template <int KV>
+__device__ __forceinline__ uint32_t fp8_hi(uint32_t w) {
+  if constexpr (KV == kKvE5M2) {
+    return __byte_perm(w, 0u, 0x3424);
+  } else {
+    return ptx::e4m3x2_to_f16x2(w >> 16);
+  }
+}
+
 // Output column d of fragment element e of O n-tile n held by lane (cq = lane
 // & 3).  The FP8 path permutes columns so that its V bytes are contiguous.
 template <bool kFp8, int D>
@@ -370,7 +397,7 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
                                            const DecodeParams& p, int u,
                                            int bq, int j, bool whole, int cta) {
   using C = Cfg<KV, D, HB>;
-  constexpr bool kFp8 = (KV == kKvE4M3);
+  constexpr bool kFp8 = is_fp8(KV);
   constexpr int kPos = C::kOTiles * 4 * 32;  // fragment positions per warp
   constexpr int kW = kGroups * C::kWarpsPerBlock;  // warps per head block
   const int kvh = j / p.NHC, hc = j % p.NHC;
@@ -462,7 +489,7 @@ __device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
                                              int u, int b, int j, int cf,
                                              int cl) {
   using C = Cfg<KV, D, HB>;
-  constexpr bool kFp8 = (KV == kKvE4M3);
+  constexpr bool kFp8 = is_fp8(KV);
   constexpr int kB = 4;
   const int kvh = j / p.NHC, hc = j % p.NHC;
   const float om = kFp8 ? __ldg(p.v_scale + b * p.Hkv + kvh) : 1.f;
@@ -525,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap map_v,
                       const DecodeParams p) {
   using C = Cfg<KV, D, HB>;
-  constexpr bool kFp8 = (KV == kKvE4M3);
+  constexpr bool kFp8 = is_fp8(KV);
   constexpr bool kMmaBF16 = !kFp8 && QBF16;
   using QT = typename std::conditional<QBF16, __nv_bfloat16, __half>::type;
   constexpr int kPos = C::kOTiles * 4 * 32;  // fragment positions per warp
@@ -870,8 +897,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int ks = 0; ks < C::kQSteps; ++ks) {
-          const uint32_t b0 = ptx::e4m3x2_to_f16x2(kw[ks] & 0xffffu);
-          const uint32_t b1 = ptx::e4m3x2_to_f16x2(kw[ks] >> 16);
+          const uint32_t b0 = fp8_lo<KV>(kw[ks]);
+          const uint32_t b1 = fp8_hi<KV>(kw[ks]);
           if (C::kSplitQK && (ks & 1))
             ptx::mma16816<false>(s2[n], qf[ks], b0, b1);
           else
@@ -1013,17 +1040,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t q01 = __byte_perm(xc[wi], xd[wi], 0x5140);
           const uint32_t q23 = __byte_perm(xc[wi], xd[wi], 0x7362);
           ptx::mma16816<false>(o[4 * wi + 0], pa,
-                               ptx::e4m3x2_to_f16x2(p01 & 0xffffu),
-                               ptx::e4m3x2_to_f16x2(q01 & 0xffffu));
+                               fp8_lo<KV>(p01),
+                               fp8_lo<KV>(q01));
           ptx::mma16816<false>(o[4 * wi + 1], pa,
-                               ptx::e4m3x2_to_f16x2(p01 >> 16),
-                               ptx::e4m3x2_to_f16x2(q01 >> 16));
+                               fp8_hi<KV>(p01),
+                               fp8_hi<KV>(q01));
           ptx::mma16816<false>(o[4 * wi + 2], pa,
-                               ptx::e4m3x2_to_f16x2(p23 & 0xffffu),
-                               ptx::e4m3x2_to_f16x2(q23 & 0xffffu));
+                               fp8_lo<KV>(p23),
+                               fp8_lo<KV>(q23));
           ptx::mma16816<false>(o[4 * wi + 3], pa,
-                               ptx::e4m3x2_to_f16x2(p23 >> 16),
-                               ptx::e4m3x2_to_f16x2(q23 >> 16));
+                               fp8_hi<KV>(p23),
+                               fp8_hi<KV>(q23));
         }
       }
     }

@@ -39,6 +39,10 @@ from typing import Optional
 import torch
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
+# 8-bit cache kinds: torch dtype, largest finite value, NaN byte used as pad
+_FP8 = {"e4m3": (torch.float8_e4m3fn, E4M3_MAX, 0x7F),
+        "e5m2": (torch.float8_e5m2, E5M2_MAX, 0x7F)}
 
 _DT = {"f16": torch.float16, "bf16": torch.bfloat16}
 
@@ -53,7 +57,7 @@ class Workload:
     D: int
     Smax: int
     dtype: str = "bf16"          # q / out dtype: "f16" | "bf16"
-    kv: str = "same"             # "same" (cache in ``dtype``) | "e4m3"
+    kv: str = "same"             # "same" (cache in ``dtype``) | "e4m3" | "e5m2"
     lens: tuple = ("uniform",)   # ("uniform",) -> every seq_len = Smax,
                                  # ("fixed", L), ("ragged", lo, hi),
                                  # ("list", l0, l1, ...)
@@ -69,14 +73,14 @@ class Workload:
 
     @property
     def kv_elem_bytes(self) -> int:
-        return 1 if self.kv == "e4m3" else 2
+        return 1 if self.kv in _FP8 else 2
 
     def algorithmic_bytes(self, seq_lens) -> int:
         """K+V bytes of the valid tokens + q + out (+ FP8 scales)."""
         total_tokens = int(sum(int(x) for x in seq_lens))
         kv = 2 * self.Hkv * self.D * self.kv_elem_bytes * total_tokens
         qo = 2 * self.B * self.Hq * self.D * 2
-        sc = 2 * self.B * self.Hkv * 4 if self.kv == "e4m3" else 0
+        sc = 2 * self.B * self.Hkv * 4 if self.kv in _FP8 else 0
         return kv + qo + sc
 
     def algorithmic_flops(self, seq_lens) -> int:
@@ -108,6 +112,10 @@ WORKLOADS = {
     "ragged_fp8_b64_h32_kv8_l500_30000":
         Workload("ragged_fp8_b64_h32_kv8_l500_30000", 64, 32, 8, 128, 30000,
                  "bf16", kv="e4m3", lens=("ragged", 500, 30000), seed=1007),
+    # the same ragged batch with the other 8-bit cache format the pages name
+    "ragged_e5m2_b64_h32_kv8_l500_30000":
+        Workload("ragged_e5m2_b64_h32_kv8_l500_30000", 64, 32, 8, 128, 30000,
+                 "bf16", kv="e5m2", lens=("ragged", 500, 30000), seed=1007),
 }
 
 HEADLINE = "llama70b_b8_s8192_bf16"
@@ -154,16 +162,19 @@ def make_inputs(w: Workload, *, pad: str = "nan",
     qdt = _DT[w.dtype]
     q = torch.randn((w.B, w.Hq, w.D), generator=gen).to(qdt)
 
-    fp8 = w.kv == "e4m3"
-    cdt = torch.float8_e4m3fn if fp8 else qdt
+    fp8 = w.kv in _FP8
+    if fp8:
+        cdt, code_max, nan_code = _FP8[w.kv]
+    else:
+        cdt = qdt
     shape = (w.B, w.Hkv, w.Smax, w.D)
     if fp8:
         k = torch.empty(shape, dtype=torch.uint8)
         v = torch.empty(shape, dtype=torch.uint8)
         k_scale = torch.ones((w.B, w.Hkv), dtype=torch.float32)
         v_scale = torch.ones((w.B, w.Hkv), dtype=torch.float32)
-        k.fill_(0x7F if pad == "nan" else 0)   # 0x7F: the E4M3 NaN code
-        v.fill_(0x7F if pad == "nan" else 0)
+        k.fill_(nan_code if pad == "nan" else 0)
+        v.fill_(nan_code if pad == "nan" else 0)
     else:
         k = torch.full(shape, _pad_value(qdt, pad), dtype=cdt)
         v = torch.full(shape, _pad_value(qdt, pad), dtype=cdt)
@@ -177,16 +188,16 @@ def make_inputs(w: Workload, *, pad: str = "nan",
                 continue
             if fp8:
                 amax = x.abs().amax(dim=(1, 2))                 # [Hkv]
-                s = torch.where(amax > 0, amax / E4M3_MAX,
+                s = torch.where(amax > 0, amax / code_max,
                                 torch.ones_like(amax)).to(torch.float32)
                 sc[b] = s
-                codes = (x / s[:, None, None]).to(torch.float8_e4m3fn)
+                codes = (x / s[:, None, None]).to(cdt)
                 dst[b, :, :L, :] = codes.view(torch.uint8)
             else:
                 dst[b, :, :L, :] = x.to(cdt)
     if fp8:
-        k = k.view(torch.float8_e4m3fn)
-        v = v.view(torch.float8_e4m3fn)
+        k = k.view(cdt)
+        v = v.view(cdt)
     return {"q": q, "k": k, "v": v, "k_scale": k_scale, "v_scale": v_scale,
             "seq_lens": seq_lens, "scale": w.scale}
 

@@ -75,7 +75,8 @@ typedef enum {
 typedef enum {
   GQA_F16 = 0,  /* IEEE binary16                                  */
   GQA_BF16 = 1, /* bfloat16                                       */
-  GQA_E4M3 = 2  /* OCP FP8 E4M3 ("e4m3fn"), cache elements only   */
+  GQA_E4M3 = 2, /* OCP FP8 E4M3 ("e4m3fn"), cache elements only   */
+  GQA_E5M2 = 3  /* OCP FP8 E5M2, cache elements only             */
 } gqa_dtype;
 
 /*
@@ -98,14 +99,17 @@ gqa_status gqa_decode(const void* q, const void* k_cache, const void* v_cache,
                       void* stream);
 
 /*
- * gqa_decode_fp8 — the same step with an FP8 E4M3 cache and one fp32 scale
- * per (sequence, KV head) for K and one for V ("Grouped-Query Attention: How
- * Sharing KV Heads Shrinks Inference Memory", FP8 KV cache: an 8-bit cache
- * with scaling factors, halving the bytes read per step).  The cached value
- * of element x of K[b, j] is e4m3(x) * k_scale[b*Hkv + j] (likewise for V).
+ * gqa_decode_fp8 — the same step with an 8-bit floating-point cache and one
+ * fp32 scale per (sequence, KV head) for K and one for V ("Grouped-Query
+ * Attention: How Sharing KV Heads Shrinks Inference Memory", FP8 KV cache: an
+ * 8-bit cache with scaling factors, e4m3 or e5m2, halving the bytes read per
+ * step).  The cached value of element x of K[b, j] is
+ * decode(x) * k_scale[b*Hkv + j] (likewise for V).
  *
- *   k_cache, v_cache [B, Hkv, Smax, D] E4M3 bytes, device, 16-byte aligned
+ *   k_cache, v_cache [B, Hkv, Smax, D] 8-bit codes, device, 16-byte aligned
  *   k_scale, v_scale [B, Hkv] fp32, device, 4-byte aligned, finite
+ *   kv_dtype         GQA_E4M3 (OCP E4M3, max 448) or GQA_E5M2 (OCP E5M2,
+ *                    max 57344): the code format of both caches
  *   qo_dtype         GQA_F16 or GQA_BF16: the dtype of q and out
  * Other arguments as for gqa_decode.
  */
@@ -113,7 +117,8 @@ gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
                           const void* v_cache, const float* k_scale,
                           const float* v_scale, const int32_t* seq_lens,
                           float scale, void* out, int B, int Hq, int Hkv,
-                          int Smax, int D, gqa_dtype qo_dtype, void* stream);
+                          int Smax, int D, gqa_dtype kv_dtype,
+                          gqa_dtype qo_dtype, void* stream);
 
 /*
  * gqa_decode_static — gqa_decode without any device allocation.

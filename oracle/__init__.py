@@ -9,8 +9,8 @@ The arithmetic lives in ``gqa_oracle.c`` (plain C, fp64, plain loops); this
 module only builds it with gcc and marshals numpy arrays through ctypes.  The
 method it follows, with the passages it restates, is described in the C file's
 header: scaled dot-product attention per query head, query head h reading KV
-head floor(h / G), softmax over the valid cached tokens, optional FP8 E4M3
-cache values times a per-(sequence, KV head) scale.
+head floor(h / G), softmax over the valid cached tokens, optional FP8 E4M3 /
+E5M2 cache values times a per-(sequence, KV head) scale.
 """
 from __future__ import annotations
 
@@ -25,7 +25,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gqa_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-F16, BF16, E4M3, F64 = 0, 1, 2, 3
+F16, BF16, E4M3, F64, E5M2 = 0, 1, 2, 3, 4
 
 _lib = None
 
@@ -67,6 +67,8 @@ def _load():
     lib.oracle_bf16_to_f64.restype = f64
     lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_to_f64.restype = f64
+    lib.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e5m2_to_f64.restype = f64
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
     _lib = lib
@@ -93,6 +95,8 @@ def _as_raw(x, what):
                 return x.view(torch.uint16).numpy(), BF16
             if x.dtype == torch.float8_e4m3fn:
                 return x.view(torch.uint8).numpy(), E4M3
+            if x.dtype == torch.float8_e5m2:
+                return x.view(torch.uint8).numpy(), E5M2
             if x.dtype == torch.uint8:
                 return x.numpy(), E4M3
             x = x.double().numpy()
@@ -137,7 +141,7 @@ def gqa_decode(q, k, v, seq_lens, scale, *, k_scale=None, v_scale=None,
     """out[B, Hq, D] (float64) of one GQA decode step.
 
     q: [B, Hq, D]; k, v: [B, Hkv, Smax, D] (float16/bfloat16/float64 values, or
-    FP8 E4M3 bytes with ``k_scale``/``v_scale`` of shape [B, Hkv]);
+    FP8 E4M3 / E5M2 codes with ``k_scale``/``v_scale`` of shape [B, Hkv]);
     seq_lens: [B] valid cached tokens per sequence.
     """
     lib = _load()
@@ -221,6 +225,10 @@ def bf16_to_f64(bits: int) -> float:
 
 def e4m3_to_f64(bits: int) -> float:
     return _load().oracle_e4m3_to_f64(bits)
+
+
+def e5m2_to_f64(bits: int) -> float:
+    return _load().oracle_e5m2_to_f64(bits)
 
 
 def max_threads() -> int:

@@ -25,7 +25,8 @@
  *    decoding step attend over the cached K/V of all prior tokens).  The cache
  *    holds exactly seq_lens[b] valid tokens; the caller has appended the current
  *    token already.  A sequence with no valid token yields an all-zero output.
- *  - FP8 cache: each stored byte is an OCP FP8 E4M3 ("e4m3fn") code, the value
+ *  - FP8 cache: each stored byte is an OCP FP8 E4M3 ("e4m3fn") or E5M2 code (the
+ *    pages name both 8-bit formats), the value
  *    is decode(code) * scale with one fp32 scale per (sequence, KV head) for K
  *    and one for V ("... Shrinks Inference Memory", FP8 KV cache: 8-bit
  *    floating-point cache with scaling factors).
@@ -34,7 +35,8 @@
  *    and "Why does GQA decide your batch size?").
  *
  * Every input element is first converted to fp64 by this file's own decoders
- * (written from the IEEE binary16, bfloat16 and OCP FP8 E4M3 bit layouts);
+ * (written from the IEEE binary16, bfloat16 and OCP FP8 E4M3 / E5M2 bit
+ * layouts);
  * all arithmetic after that is fp64.  The softmax subtracts the row maximum
  * before exponentiating (a rewrite that is exact in real arithmetic).
  *
@@ -51,7 +53,7 @@
 #endif
 
 /* Element type codes understood by the oracle's loaders. */
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F64 = 3 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F64 = 3, ORC_E5M2 = 4 };
 
 /* ---------------------------------------------------------------- decoders */
 
@@ -104,11 +106,29 @@ double oracle_e4m3_to_f64(uint8_t bits) {
   return sign ? -mag : mag;
 }
 
+/* OCP FP8 E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits,
+ * IEEE-style infinities and NaNs at exponent 31, largest finite 57344. */
+double oracle_e5m2_to_f64(uint8_t bits) {
+  int sign = (bits >> 7) & 1;
+  int e = (bits >> 2) & 0x1F;
+  int f = bits & 0x3;
+  double mag;
+  if (e == 0) {
+    mag = ldexp((double)f, -16); /* subnormal: f * 2^-2 * 2^-14 */
+  } else if (e == 31) {
+    mag = (f == 0) ? INFINITY : NAN;
+  } else {
+    mag = ldexp(1.0 + (double)f / 4.0, e - 15);
+  }
+  return sign ? -mag : mag;
+}
+
 static double load_elem(const void* base, size_t idx, int dtype) {
   switch (dtype) {
     case ORC_F16: return oracle_f16_to_f64(((const uint16_t*)base)[idx]);
     case ORC_BF16: return oracle_bf16_to_f64(((const uint16_t*)base)[idx]);
     case ORC_E4M3: return oracle_e4m3_to_f64(((const uint8_t*)base)[idx]);
+    case ORC_E5M2: return oracle_e5m2_to_f64(((const uint8_t*)base)[idx]);
     case ORC_F64: return ((const double*)base)[idx];
     default: return NAN;
   }
@@ -195,9 +215,9 @@ static int check_problem(const orc_problem* p) {
   if (!p->q || !p->k || !p->v || !p->seq_lens) return 1;
   if (p->B < 0 || p->Hq < 1 || p->Hkv < 1 || p->Smax < 1 || p->D < 1) return 1;
   if (p->Hq % p->Hkv != 0) return 1;
-  if (p->q_dtype == ORC_E4M3) return 1;
-  if (p->q_dtype < 0 || p->q_dtype > ORC_F64) return 1;
-  if (p->kv_dtype < 0 || p->kv_dtype > ORC_F64) return 1;
+  if (p->q_dtype == ORC_E4M3 || p->q_dtype == ORC_E5M2) return 1;
+  if (p->q_dtype < 0 || p->q_dtype > ORC_E5M2) return 1;
+  if (p->kv_dtype < 0 || p->kv_dtype > ORC_E5M2) return 1;
   return 0;
 }
 

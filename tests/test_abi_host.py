@@ -70,9 +70,10 @@ def _call(q=A, k=A * 2, v=A * 3, lens=A * 4, scale=0.125, out=A * 5, B=2,
 
 
 def _call8(q=A, k=A * 2, v=A * 3, ks=A * 6, vs=A * 7, lens=A * 4, scale=0.125,
-           out=A * 5, B=2, Hq=8, Hkv=2, Smax=128, D=64, dtype=gq.GQA_BF16):
+           out=A * 5, B=2, Hq=8, Hkv=2, Smax=128, D=64, kv=gq.GQA_E4M3,
+           dtype=gq.GQA_BF16):
     return gq.lib().gqa_decode_fp8(q, k, v, ks, vs, lens, scale, out, B, Hq,
-                                   Hkv, Smax, D, dtype, None)
+                                   Hkv, Smax, D, kv, dtype, None)
 
 
 @pytest.mark.parametrize("kw", [
@@ -96,6 +97,8 @@ def test_decode_unsupported_head_dim(L, kw):
 @pytest.mark.parametrize("kw", [
     dict(ks=None), dict(vs=None), dict(ks=A * 6 + 2), dict(q=None),
     dict(dtype=gq.GQA_E4M3), dict(Hq=6, Hkv=4), dict(scale=0.0),
+    dict(kv=gq.GQA_BF16), dict(kv=gq.GQA_F16), dict(kv=9),
+    dict(kv=gq.GQA_E5M2, ks=None), dict(kv=gq.GQA_E5M2, B=0),
 ])
 def test_decode_fp8_rejects_invalid_arguments(L, kw):
     assert _call8(**kw) == gq.GQA_ERR_INVALID_ARG

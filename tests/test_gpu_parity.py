@@ -54,6 +54,10 @@ CASES = [
     ("fp8_f16_q_g4", 2, 16, 4, 128, 150, "f16", "e4m3", ("list", 150, 80)),
     ("fp8_mqa_g64", 1, 64, 1, 128, 300, "bf16", "e4m3", ("uniform",)),
     ("fp8_mha_g1", 2, 4, 4, 64, 99, "bf16", "e4m3", ("list", 99, 17)),
+    ("e5m2_g4_d128_ragged", 4, 32, 8, 128, 400, "bf16", "e5m2",
+     ("list", 400, 1, 70, 333)),
+    ("e5m2_g8_d64_f16", 2, 16, 2, 64, 300, "f16", "e5m2", ("list", 300, 129)),
+    ("e5m2_mqa_g64", 1, 64, 1, 128, 200, "bf16", "e5m2", ("uniform",)),
     # more sequences than threads per block: the general scheduler prologue
     ("bf16_many_sequences", 300, 8, 2, 64, 70, "bf16", "same",
      ("ragged", 0, 70)),

@@ -2,7 +2,8 @@
 
 * the pages' worked example (golden fixture, printed to 4 decimals);
 * the pages' cache-size figures (closed form);
-* library routines: torch's float16 / bfloat16 / float8_e4m3fn conversions and
+* library routines: torch's float16 / bfloat16 / float8_e4m3fn / float8_e5m2
+  conversions and
   torch's scaled_dot_product_attention (``enable_gqa=True``) in float64;
 * structural facts the pages state: G = 1 is MHA, GQA equals MHA on a
   repeat_kv-expanded cache, query head h reads KV head floor(h / G), heads that
@@ -144,6 +145,19 @@ def test_e4m3_decoder_matches_torch(oracle_mod):
     assert oracle_mod.e4m3_to_f64(0x01) == 2.0 ** -9
 
 
+def test_e5m2_decoder_matches_torch(oracle_mod):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e5m2).double().numpy()
+    ours = np.array([oracle_mod.e5m2_to_f64(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert nan.sum() == 6                      # S.11111.{01,10,11}
+    assert np.array_equal(nan, np.isnan(ours))
+    assert np.array_equal(ref[~nan], ours[~nan])
+    assert oracle_mod.e5m2_to_f64(0x7B) == 57344.0
+    assert oracle_mod.e5m2_to_f64(0x7C) == np.inf
+    assert oracle_mod.e5m2_to_f64(0x01) == 2.0 ** -16
+
+
 # ------------------------------------------------- library routine: SDPA
 
 def _sdpa_gqa(inp):
@@ -172,6 +186,8 @@ SMALL = [
     Workload("t_mqa", 2, 16, 1, 64, 50, "bf16", lens=("ragged", 1, 50), seed=10),
     Workload("t_fp8", 3, 8, 2, 128, 90, "bf16", kv="e4m3",
              lens=("ragged", 1, 90), seed=11),
+    Workload("t_e5m2", 3, 8, 2, 128, 90, "bf16", kv="e5m2",
+             lens=("ragged", 1, 90), seed=12),
 ]
 
 
