@@ -260,6 +260,10 @@ def main(argv=None):
     gq.lib()
 
     inp = make_inputs(w, pad="zero", seed=w.seed + rank)
+    # a paged workload also carries its contiguous copy (for checks): not an
+    # input of the step
+    inp.pop("k_contig", None)
+    inp.pop("v_contig", None)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
          for k, v in inp.items()}
     out = torch.empty_like(d["q"])

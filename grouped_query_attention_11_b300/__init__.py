@@ -11,6 +11,8 @@ its names:
 * :func:`gqa_decode` — one decode step with a float16 / bfloat16 cache;
 * :func:`gqa_decode_fp8` — the same with an FP8 E4M3 cache and per-(sequence,
   KV head) scales;
+* :func:`gqa_decode_paged` — the same over a paged cache (page pool + block
+  table);
 * :func:`gqa_decode_static` — gqa_decode with a fixed scratch array instead of
   any device allocation;
 * :func:`gqa_kv_bytes_per_token`, :func:`gqa_status_string`,
@@ -37,6 +39,9 @@ SIGNATURES = {
                           _I32, _I32, _I32, _VP]),
     "gqa_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
                               _I32, _I32, _I32, _I32, _I32, _I32, _VP]),
+    "gqa_decode_paged": (_I32, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
+                                _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                _VP]),
     "gqa_decode_static": (_I32, [_VP, _VP, _VP, _VP, _F32, _VP, _I32, _I32,
                                  _I32, _I32, _I32, _I32, _VP]),
     "gqa_kv_bytes_per_token": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
@@ -167,6 +172,42 @@ def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out=None,
     return out
 
 
+def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens,
+                     scale: float, out=None, stream=None):
+    """GQA decode over a paged cache; returns ``out`` [B, Hq, D].
+
+    k_pages / v_pages [num_pages, Hkv, page_size, D] (q's 16-bit dtype),
+    block_table [B, max_pages] int32 (page of tokens [i*page_size,
+    (i+1)*page_size) of sequence b), seq_lens [B] int32; page_size a
+    multiple of 64.
+    """
+    import torch
+    for n, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
+                 ("block_table", block_table), ("seq_lens", seq_lens)):
+        _check_dev(n, t)
+    if k_pages.dtype != q.dtype or v_pages.dtype != q.dtype:
+        raise TypeError("q, k_pages and v_pages must share a dtype")
+    if seq_lens.dtype != torch.int32 or block_table.dtype != torch.int32:
+        raise TypeError("seq_lens and block_table must be int32")
+    if v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape")
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _check_dev("out", out)
+    st = lib().gqa_decode_paged(q.data_ptr(), k_pages.data_ptr(),
+                                v_pages.data_ptr(), block_table.data_ptr(),
+                                seq_lens.data_ptr(), float(scale),
+                                out.data_ptr(), B, Hq, Hkv, num_pages,
+                                page_size, max_pages, D, _dtype_code(q),
+                                _stream_handle(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_decode_paged")
+    return out
+
+
 def gqa_decode_static(q, k_cache, v_cache, seq_lens, scale: float, out=None,
                       stream=None):
     """gqa_decode that allocates no device memory (fixed 16 MiB scratch kept
@@ -246,8 +287,13 @@ class BoundDecode:
 
     def __init__(self, inp: dict, out, stream=None):
         fp8 = inp.get("k_scale") is not None
+        paged = inp.get("block_table") is not None
         # run the full checks once, through the public entry points
-        if fp8:
+        if paged:
+            gqa_decode_paged(inp["q"], inp["k"], inp["v"], inp["block_table"],
+                             inp["seq_lens"], inp["scale"], out=out,
+                             stream=stream)
+        elif fp8:
             gqa_decode_fp8(inp["q"], inp["k"], inp["v"], inp["k_scale"],
                            inp["v_scale"], inp["seq_lens"], inp["scale"],
                            out=out, stream=stream)
@@ -258,7 +304,15 @@ class BoundDecode:
         B, Hq, D = q.shape
         _, Hkv, Smax, _ = k.shape
         h = _stream_handle(stream)
-        if fp8:
+        if paged:
+            num_pages, _, page_size, _ = k.shape
+            self._fn = lib().gqa_decode_paged
+            self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),
+                          inp["block_table"].data_ptr(),
+                          inp["seq_lens"].data_ptr(), float(inp["scale"]),
+                          out.data_ptr(), B, Hq, Hkv, num_pages, page_size,
+                          inp["block_table"].shape[1], D, _dtype_code(q), h)
+        elif fp8:
             self._fn = lib().gqa_decode_fp8
             self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),
                           inp["k_scale"].data_ptr(), inp["v_scale"].data_ptr(),
@@ -282,6 +336,10 @@ class BoundDecode:
 def decode_inputs(inp: dict, out=None, stream=None):
     """Runs the right entry point on a dict of CUDA tensors (the layout the
     input generator produces, moved to the device)."""
+    if inp.get("block_table") is not None:
+        return gqa_decode_paged(inp["q"], inp["k"], inp["v"],
+                                inp["block_table"], inp["seq_lens"],
+                                inp["scale"], out=out, stream=stream)
     if inp.get("k_scale") is not None:
         return gqa_decode_fp8(inp["q"], inp["k"], inp["v"], inp["k_scale"],
                               inp["v_scale"], inp["seq_lens"], inp["scale"],

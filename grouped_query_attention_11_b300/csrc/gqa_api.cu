@@ -98,26 +98,30 @@ struct Variant {
   int smem;
 };
 
-template <int KV, bool QB, int D, int HB>
+template <int KV, bool QB, int D, int HB, bool PG>
 Variant variant() {
-  return {&gqa_decode_kernel<KV, QB, D, HB>, Cfg<KV, D, HB>::kSmemBytes};
+  return {&gqa_decode_kernel<KV, QB, D, HB, PG>, Cfg<KV, D, HB>::kSmemBytes};
 }
 
-template <int KV, bool QB, int D>
+template <int KV, bool QB, int D, bool PG>
 Variant pick_hb(int hb) {
   switch (hb) {
-    case 1: return variant<KV, QB, D, 1>();
-    case 2: return variant<KV, QB, D, 2>();
-    default: return variant<KV, QB, D, 4>();
+    case 1: return variant<KV, QB, D, 1, PG>();
+    case 2: return variant<KV, QB, D, 2, PG>();
+    default: return variant<KV, QB, D, 4, PG>();
   }
 }
 
-template <int KV, bool QB>
+template <int KV, bool QB, bool PG = false>
 Variant pick_d(int D, int hb) {
-  return D == 64 ? pick_hb<KV, QB, 64>(hb) : pick_hb<KV, QB, 128>(hb);
+  return D == 64 ? pick_hb<KV, QB, 64, PG>(hb) : pick_hb<KV, QB, 128, PG>(hb);
 }
 
-Variant pick(int kv, bool q_bf16, int D, int hb) {
+// Paged caches are instantiated for the 16-bit element types.
+Variant pick(int kv, bool q_bf16, int D, int hb, bool paged = false) {
+  if (paged)
+    return kv == kKvBF16 ? pick_d<kKvBF16, true, true>(D, hb)
+                         : pick_d<kKvF16, false, true>(D, hb);
   if (kv == kKvF16) return pick_d<kKvF16, false>(D, hb);
   if (kv == kKvBF16) return pick_d<kKvBF16, true>(D, hb);
   if (kv == kKvE5M2)
@@ -245,11 +249,16 @@ gqa_status check_common(const void* q, const void* k, const void* v,
   return GQA_OK;
 }
 
+// Smax: the cache's token capacity per sequence.  A paged cache passes its
+// block table, page size and page count (Smax = max_pages * page_size);
+// block_table == nullptr is a contiguous cache.
 gqa_status launch(const void* q, const void* k, const void* v,
                   const float* k_scale, const float* v_scale,
                   const int32_t* seq_lens, float scale, void* out, int B,
                   int Hq, int Hkv, int Smax, int D, int kv_kind, bool q_bf16,
-                  void* stream_ptr) {
+                  void* stream_ptr, const int32_t* block_table = nullptr,
+                  int page_size = 0, int num_pages = 0) {
+  const bool paged = block_table != nullptr;
   t_last_launches = 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int G = Hq / Hkv;
@@ -260,13 +269,17 @@ gqa_status launch(const void* q, const void* k, const void* v,
   const long long units = static_cast<long long>(B) * Hkv * NHC;
   if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
 
-  const Variant var = pick(kv_kind, q_bf16, D, hb);
+  const Variant var = pick(kv_kind, q_bf16, D, hb, paged);
   const int elem_bytes = is_fp8(kv_kind) ? 1 : 2;
+  // the TMA view [planes][rows][D]: (B*Hkv, Smax) or (num_pages*Hkv,
+  // page_size)
+  const int planes_outer = paged ? num_pages : B;
+  const int rows = paged ? page_size : Smax;
 
   std::lock_guard<std::mutex> lock(g_mu);
   CUtensorMap map_k, map_v;
-  if (!cached_cache_map(&map_k, k, elem_bytes, B, Hkv, Smax, D) ||
-      !cached_cache_map(&map_v, v, elem_bytes, B, Hkv, Smax, D))
+  if (!cached_cache_map(&map_k, k, elem_bytes, planes_outer, Hkv, rows, D) ||
+      !cached_cache_map(&map_v, v, elem_bytes, planes_outer, Hkv, rows, D))
     return GQA_ERR_CUDA;
 
   int dev = 0;
@@ -292,7 +305,7 @@ gqa_status launch(const void* q, const void* k, const void* v,
   uint8_t* ctl = static_cast<uint8_t*>(sc->ctl);
   uint8_t* part = static_cast<uint8_t*>(sc->part);
 
-  DecodeParams p;
+  DecodeParams p = {};
   p.q = q;
   p.out = out;
   p.seq_lens = seq_lens;
@@ -310,6 +323,10 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.G = G;
   p.NHC = NHC;
   p.R = R;
+  p.block_table = block_table;
+  p.max_pages = paged ? Smax / page_size : 0;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
 
   // Programmatic dependent launch: the kernel may start launching while the
   // previous kernel in the stream finishes; it waits (griddepcontrol.wait)
@@ -415,7 +432,7 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
   if (cudaMemsetAsync(wb, 0, kHeaderBytes + cnt_bytes, stream) != cudaSuccess)
     return GQA_ERR_CUDA;
 
-  DecodeParams p;
+  DecodeParams p = {};
   p.q = q;
   p.out = out;
   p.seq_lens = seq_lens;
@@ -532,6 +549,37 @@ gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
 void gqa_set_num_ctas(int num_ctas) {
   std::lock_guard<std::mutex> lock(gqa::g_mu);
   gqa::g_num_ctas_override = num_ctas > 0 ? num_ctas : 0;
+}
+
+gqa_status gqa_decode_paged(const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* block_table,
+                            const int32_t* seq_lens, float scale, void* out,
+                            int B, int Hq, int Hkv, int num_pages,
+                            int page_size, int max_pages, int D,
+                            gqa_dtype dtype, void* stream) {
+  gqa::t_last_launches = 0;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (!block_table || !gqa::aligned(block_table, 4)) return GQA_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_pages < 1 || page_size < 1)
+    return GQA_ERR_INVALID_ARG;
+  if (page_size % gqa::kTileTokens != 0) return GQA_ERR_UNSUPPORTED;
+  const long long smax = static_cast<long long>(max_pages) * page_size;
+  if (smax > INT32_MAX ||
+      static_cast<long long>(num_pages) * Hkv > INT32_MAX)
+    return GQA_ERR_UNSUPPORTED;
+  const gqa_status st =
+      gqa::check_common(q, k_pages, v_pages, seq_lens, scale, out, B, Hq, Hkv,
+                        static_cast<int>(smax), D);
+  if (st != GQA_OK) return st;
+  try {
+    return gqa::launch(q, k_pages, v_pages, nullptr, nullptr, seq_lens, scale,
+                       out, B, Hq, Hkv, static_cast<int>(smax), D,
+                       dtype == GQA_BF16 ? gqa::kKvBF16 : gqa::kKvF16,
+                       dtype == GQA_BF16, stream, block_table, page_size,
+                       num_pages);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
 }
 
 gqa_status gqa_decode_static(const void* q, const void* k_cache,

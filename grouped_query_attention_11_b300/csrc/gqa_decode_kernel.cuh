@@ -50,6 +50,9 @@
 //    bumps a per-unit counter; the block that arrives last merges all
 //    partials of the unit (after its own last unit) and writes the output,
 //    then resets the counter.  No block ever waits on another block.
+//  * Paged cache (PAGED).  Only the producer changes: each tile's page comes
+//    from the block table and the TMA load addresses (row in page, page x
+//    Hkv + KV head) of the page pool [pages x Hkv][page_size][D].
 //  * Every mbarrier wait gives up after a time limit, sets an error flag the
 //    host can query, and lets the block finish without hanging the GPU.
 #pragma once
@@ -97,7 +100,10 @@ __host__ __device__ constexpr bool is_fp8(int kv) {
   return kv == kKvE4M3 || kv == kKvE5M2;
 }
 
-enum ErrorBits : uint32_t { kErrWaitTimeout = 1u };
+enum ErrorBits : uint32_t {
+  kErrWaitTimeout = 1u,  // a pipeline wait gave up after its time limit
+  kErrBadPage = 2u,      // a block-table entry outside [0, num_pages)
+};
 
 struct DecodeParams {
   const void* q;            // [B, Hq, D] f16 / bf16
@@ -109,6 +115,10 @@ struct DecodeParams {
   float* part_lse;          // [slots, rows_pad]     log2-sum-exp of partials
   uint32_t* counters;       // [units] arrivals per unit (zero between calls)
   uint32_t* error;          // fault flags
+  // paged cache only: block_table[b * max_pages + i] is the page holding
+  // tokens [i * page_size, (i + 1) * page_size) of sequence b
+  const int32_t* block_table;
+  int max_pages, page_size, num_pages;
   float scale_log2;         // softmax scale * log2(e)
   int B, Hq, Hkv, Smax, G;
   int NHC;                  // head chunks per KV head
@@ -546,7 +556,7 @@ __device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
   if (t == 0) p.counters[u] = 0u;
 }
 
-template <int KV, bool QBF16, int D, int HB>
+template <int KV, bool QBF16, int D, int HB, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v,
@@ -708,16 +718,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (s_abort) break;
         ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-        const int plane = w.b * p.Hkv + w.j / p.NHC;
+        const int kvh = w.j / p.NHC;
         const int tok = w.ti * kTileTokens;
+        // tile coordinates in the cache view [planes][tokens][D]
+        int row = tok, plane = w.b * p.Hkv + kvh;
+        if constexpr (PAGED) {
+          // a tile lies inside one page (page_size is a multiple of it)
+          int pg = __ldg(p.block_table +
+                         static_cast<size_t>(w.b) * p.max_pages +
+                         tok / p.page_size);
+          if (pg < 0 || pg >= p.num_pages) {
+            atomicOr(p.error, kErrBadPage);
+            pg = 0;
+          }
+          row = tok % p.page_size;
+          plane = pg * p.Hkv + kvh;
+        }
         uint8_t* ks = ring + stage * C::kStageBytes;
         uint8_t* vs = ks + C::kTileBytes;
 #pragma unroll
         for (int bx = 0; bx < C::kBoxesPerTile; ++bx) {
           ptx::tma_load_3d(ks + bx * C::kBoxBytes, &map_k, &full[stage],
-                           bx * C::kBoxElems, tok, plane, policy);
+                           bx * C::kBoxElems, row, plane, policy);
           ptx::tma_load_3d(vs + bx * C::kBoxBytes, &map_v, &full[stage],
-                           bx * C::kBoxElems, tok, plane, policy);
+                           bx * C::kBoxElems, row, plane, policy);
         }
         w.next(p, HU);
       }

@@ -62,6 +62,7 @@ class Workload:
                                  # ("fixed", L), ("ragged", lo, hi),
                                  # ("list", l0, l1, ...)
     seed: int = 1000
+    page_size: int = 0           # > 0: paged cache with pages of this size
 
     @property
     def G(self) -> int:
@@ -112,6 +113,11 @@ WORKLOADS = {
     "ragged_fp8_b64_h32_kv8_l500_30000":
         Workload("ragged_fp8_b64_h32_kv8_l500_30000", 64, 32, 8, 128, 30000,
                  "bf16", kv="e4m3", lens=("ragged", 500, 30000), seed=1007),
+    # the 70B-shaped decode over a paged cache of 64-token pages (one page per
+    # tile: every tile's page comes from the block table)
+    "llama70b_paged64_b8_s8192_bf16":
+        Workload("llama70b_paged64_b8_s8192_bf16", 8, 64, 8, 128, 8192,
+                 "bf16", seed=1003, page_size=64),
     # the same ragged batch with the other 8-bit cache format the pages name
     "ragged_e5m2_b64_h32_kv8_l500_30000":
         Workload("ragged_e5m2_b64_h32_kv8_l500_30000", 64, 32, 8, 128, 30000,
@@ -198,8 +204,45 @@ def make_inputs(w: Workload, *, pad: str = "nan",
     if fp8:
         k = k.view(cdt)
         v = v.view(cdt)
-    return {"q": q, "k": k, "v": v, "k_scale": k_scale, "v_scale": v_scale,
-            "seq_lens": seq_lens, "scale": w.scale}
+    out = {"q": q, "k": k, "v": v, "k_scale": k_scale, "v_scale": v_scale,
+           "seq_lens": seq_lens, "scale": w.scale}
+    if w.page_size > 0:
+        out.update(to_pages(k, v, seq_lens, w.page_size, gen, pad))
+    return out
+
+
+def to_pages(k, v, seq_lens, page_size: int, gen: torch.Generator,
+             pad: str = "nan") -> dict:
+    """Scatter contiguous caches [B, Hkv, Smax, D] into a shuffled page pool
+    [num_pages, Hkv, page_size, D] with a block table [B, max_pages] (int32,
+    -1 where a sequence has no page).  A few spare pages hold the pad value."""
+    B, Hkv, Smax, D = k.shape
+    max_pages = -(-Smax // page_size)
+    num_pages = B * max_pages + max(2, B)
+    perm = torch.randperm(num_pages, generator=gen)[:B * max_pages]
+    perm = perm.view(B, max_pages).to(torch.int32)
+    fill = _pad_value(k.dtype, pad) if k.dtype.itemsize == 2 else None
+    shape = (num_pages, Hkv, page_size, D)
+    if fill is None:   # 8-bit codes: fill through a byte view
+        kp = torch.zeros(shape, dtype=torch.uint8)
+        vp = torch.zeros(shape, dtype=torch.uint8)
+        kp.fill_(0x7F if pad == "nan" else 0)
+        vp.fill_(0x7F if pad == "nan" else 0)
+        kp, vp = kp.view(k.dtype), vp.view(k.dtype)
+    else:
+        kp = torch.full(shape, fill, dtype=k.dtype)
+        vp = torch.full(shape, fill, dtype=k.dtype)
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    for b in range(B):
+        n = -(-int(seq_lens[b]) // page_size)
+        for i in range(n):
+            pg = int(perm[b, i])
+            lo, hi = i * page_size, min((i + 1) * page_size, Smax)
+            kp[pg, :, :hi - lo] = k[b, :, lo:hi]
+            vp[pg, :, :hi - lo] = v[b, :, lo:hi]
+            table[b, i] = pg
+    return {"k": kp, "v": vp, "block_table": table, "k_contig": k,
+            "v_contig": v}
 
 
 def small_variant(w: Workload, *, B: Optional[int] = None,

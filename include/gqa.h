@@ -121,6 +121,38 @@ gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
                           gqa_dtype qo_dtype, void* stream);
 
 /*
+ * gqa_decode_paged — gqa_decode over a paged KV cache: the cache lives in a
+ * pool of fixed-size pages and a block table maps each sequence's token
+ * ranges to pages ("Grouped-Query Attention: How Sharing KV Heads Shrinks
+ * Inference Memory", Serving knobs: KV blocks; the paged kernels of serving
+ * engines that "Grouped Query Attention: Why 8 KV Heads Decide Your Batch
+ * Size" names in the repeat_kv trap).  Same arithmetic and output as
+ * gqa_decode on the cache the pages describe.
+ *
+ *   k_pages, v_pages [num_pages, Hkv, page_size, D] dtype, device, 16-byte
+ *                    aligned: page p holds page_size consecutive tokens of
+ *                    every KV head of one sequence
+ *   block_table      [B, max_pages] int32, device, 4-byte aligned: entry
+ *                    (b, i) is the page holding tokens [i*page_size,
+ *                    (i+1)*page_size) of sequence b; only entries
+ *                    i < ceil(seq_lens[b] / page_size) are read, and each
+ *                    must be in [0, num_pages)
+ *   seq_lens         [B] int32, device: valid tokens, clamped to
+ *                    [0, max_pages * page_size]
+ *   page_size        a multiple of 64 (GQA_ERR_UNSUPPORTED otherwise)
+ *   dtype            GQA_F16 or GQA_BF16
+ * Other arguments as for gqa_decode.  A block-table entry outside
+ * [0, num_pages) is not dereferenced: page 0 is read instead and bit 1 of
+ * gqa_device_errors is set.
+ */
+gqa_status gqa_decode_paged(const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* block_table,
+                            const int32_t* seq_lens, float scale, void* out,
+                            int B, int Hq, int Hkv, int num_pages,
+                            int page_size, int max_pages, int D,
+                            gqa_dtype dtype, void* stream);
+
+/*
  * gqa_decode_static — gqa_decode without any device allocation.
  *
  * The pages have no counterpart to this call.  It is for callers that cannot
@@ -173,7 +205,8 @@ const char* gqa_status_string(gqa_status status);
  * gqa_device_errors — synchronises `stream`, then returns (and clears) the
  * fault flags the kernels raised on it since the last query: 0 when none.
  * Bit 0: a pipeline wait gave up after its time limit (the affected outputs
- * are unspecified).  Returns GQA_ERR_CUDA if the synchronisation fails.
+ * are unspecified).  Bit 1: a paged call met a block-table entry outside
+ * [0, num_pages).  Returns GQA_ERR_CUDA if the synchronisation fails.
  */
 gqa_status gqa_device_errors(void* stream, uint32_t* flags);
 

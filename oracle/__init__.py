@@ -165,6 +165,47 @@ def gqa_decode(q, k, v, seq_lens, scale, *, k_scale=None, v_scale=None,
     return out
 
 
+def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale, *,
+                     nthreads: int = 0) -> np.ndarray:
+    """out[B, Hq, D] (float64) of one decode step over a paged cache.
+
+    k_pages, v_pages: [num_pages, Hkv, page_size, D]; block_table: [B,
+    max_pages], entry (b, i) the page of tokens [i*page_size, (i+1)*page_size)
+    of sequence b.  The pages of each sequence are gathered back into a
+    contiguous cache (tokens in order) and the contiguous oracle runs on it.
+    """
+    ka, kt = _as_raw(k_pages, "k_pages")
+    va, vt = _as_raw(v_pages, "v_pages")
+    table = block_table.cpu().numpy() if hasattr(block_table, "cpu") \
+        else np.asarray(block_table)
+    table = np.ascontiguousarray(table, dtype=np.int32)
+    lens = _lens(seq_lens)
+    _, Hkv, page_size, D = ka.shape
+    B, max_pages = table.shape
+    Smax = max_pages * page_size
+    kc = np.zeros((B, Hkv, Smax, D), dtype=ka.dtype)
+    vc = np.zeros((B, Hkv, Smax, D), dtype=va.dtype)
+    for b in range(B):
+        L = min(max(int(lens[b]), 0), Smax)
+        for i in range(-(-L // page_size)):
+            pg = int(table[b, i])
+            if not 0 <= pg < ka.shape[0]:
+                raise ValueError(f"block_table[{b}, {i}] = {pg} out of range")
+            kc[b, :, i * page_size:(i + 1) * page_size] = ka[pg]
+            vc[b, :, i * page_size:(i + 1) * page_size] = va[pg]
+    qa, qt = _as_raw(q, "q")
+    lib = _load()
+    B2, Hq, D2 = qa.shape
+    out = np.zeros((B2, Hq, D2), dtype=np.float64)
+    lens_c = np.minimum(np.maximum(lens, 0), Smax).astype(np.int32)
+    rc = lib.oracle_gqa_decode(_ptr(qa), qt, _ptr(kc), _ptr(vc), kt, None,
+                               None, _ptr(lens_c), float(scale), _ptr(out),
+                               B2, Hq, Hkv, Smax, D2, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gqa_decode rejected its arguments")
+    return out
+
+
 def gqa_decode_rows(q, k, v, seq_lens, scale, bh, *, k_scale=None,
                     v_scale=None, nthreads: int = 0) -> np.ndarray:
     """Output rows [n, D] (float64) for the (b, h) pairs in ``bh`` ([n, 2])."""

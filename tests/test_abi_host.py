@@ -117,3 +117,27 @@ def test_product_path_has_no_oracle_dependency():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text
                 assert "liboracle" not in text and "gqa_oracle" not in text
+
+
+def _callp(q=A, k=A * 2, v=A * 3, bt=A * 8, lens=A * 4, scale=0.125,
+           out=A * 5, B=2, Hq=8, Hkv=2, num_pages=16, page_size=64,
+           max_pages=4, D=64, dtype=gq.GQA_BF16):
+    return gq.lib().gqa_decode_paged(q, k, v, bt, lens, scale, out, B, Hq, Hkv,
+                                     num_pages, page_size, max_pages, D, dtype,
+                                     None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(bt=None), dict(bt=A * 8 + 2), dict(num_pages=0), dict(max_pages=0),
+    dict(page_size=0), dict(q=None), dict(dtype=gq.GQA_E4M3), dict(Hq=6, Hkv=4),
+    dict(scale=0.0), dict(B=0),
+])
+def test_decode_paged_rejects_invalid_arguments(L, kw):
+    assert _callp(**kw) == gq.GQA_ERR_INVALID_ARG
+    assert gq.gqa_last_launch_count() == 0
+
+
+@pytest.mark.parametrize("kw", [dict(page_size=32), dict(page_size=100),
+                                dict(D=96)])
+def test_decode_paged_unsupported(L, kw):
+    assert _callp(**kw) == gq.GQA_ERR_UNSUPPORTED

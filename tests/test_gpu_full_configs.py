@@ -42,7 +42,9 @@ def test_full_size_sampled_rows(oracle_mod, name):
     assert gq.gqa_device_errors() == 0
     assert torch.isfinite(out).all()
     pairs = sample_rows(w, inp["seq_lens"], seed=w.seed)
-    ref = oracle_mod.gqa_decode_rows(inp["q"], inp["k"], inp["v"],
+    k = inp.get("k_contig", inp["k"])   # a paged cache, gathered
+    v = inp.get("v_contig", inp["v"])
+    ref = oracle_mod.gqa_decode_rows(inp["q"], k, v,
                                      inp["seq_lens"], inp["scale"], pairs,
                                      k_scale=inp["k_scale"],
                                      v_scale=inp["v_scale"])

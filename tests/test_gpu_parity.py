@@ -302,3 +302,44 @@ def test_scratch_reuse_across_unit_counts(oracle_mod):
         inp = make_inputs(w, pad="nan")
         out = run_cuda(inp)
         assert_contract(out, oracle_full(oracle_mod, inp), w.name)
+
+
+PAGED = [
+    # name, B, Hq, Hkv, D, Smax, dtype, page_size, lens
+    ("paged64_bf16_g8", 3, 64, 8, 128, 700, "bf16", 64, ("list", 700, 1, 333)),
+    ("paged128_f16_g4", 4, 16, 4, 64, 500, "f16", 128,
+     ("list", 500, 0, 129, 255)),
+    ("paged256_bf16_mqa", 2, 64, 1, 128, 1024, "bf16", 256,
+     ("list", 1024, 257)),
+    ("paged64_bf16_mha", 2, 8, 8, 128, 200, "bf16", 64, ("list", 200, 64)),
+]
+
+
+@pytest.mark.parametrize("case", PAGED, ids=[c[0] for c in PAGED])
+def test_parity_paged(oracle_mod, case):
+    name, B, Hq, Hkv, D, Smax, dt, ps, lens = case
+    w = Workload(name, B, Hq, Hkv, D, Smax, dt, lens=lens,
+                 seed=3000 + PAGED.index(case), page_size=ps)
+    inp = make_inputs(w, pad="nan")
+    out = run_cuda(inp)
+    ref = oracle_mod.gqa_decode_paged(inp["q"], inp["k"], inp["v"],
+                                      inp["block_table"], inp["seq_lens"],
+                                      inp["scale"])
+    assert_close(out, ref, name)
+    # the same cache laid out contiguously gives the same bits
+    flat = {k: v for k, v in inp.items() if k != "block_table"}
+    flat["k"], flat["v"] = inp["k_contig"], inp["v_contig"]
+    assert torch.equal(run_cuda(flat).view(torch.int16),
+                       out.view(torch.int16))
+
+
+def test_paged_bad_block_table_entry_is_flagged():
+    w = Workload("pgbad", 2, 16, 2, 64, 256, "bf16", lens=("list", 256, 200),
+                 seed=3100, page_size=64)
+    inp = make_inputs(w, pad="nan")
+    inp["block_table"] = inp["block_table"].clone()
+    inp["block_table"][1, 2] = 10 ** 6     # read: tokens 128..191 of seq 1
+    dev = to_device(inp)
+    gq.decode_inputs(dev)
+    assert gq.gqa_device_errors() & 2
+    assert gq.gqa_device_errors() == 0     # the query cleared it

@@ -386,3 +386,40 @@ def test_sampled_rows_match_full_decode(oracle_mod):
                                       inp["seq_lens"], inp["scale"], bh)
     for i, (b, h) in enumerate(bh):
         assert np.array_equal(rows[i], full[b, h])
+
+
+# ------------------------------------------------- paged cache (gather step)
+
+def test_paged_oracle_on_worked_example_in_reversed_pages(oracle_mod):
+    """The worked example's two cached tokens stored in a page pool in
+    reverse order (page size 1, so token t of KV head j sits in page 1 - t)
+    give the printed outputs."""
+    Q, K, V, scale, W, O, tol = _read_golden(GOLDEN)
+    # pool [num_pages=2, Hkv=2, page_size=1, D=2]: page p holds token 1 - p
+    kp = np.zeros((2, 2, 1, 2))
+    vp = np.zeros((2, 2, 1, 2))
+    for t in range(2):
+        kp[1 - t, :, 0] = K[0, :, t]
+        vp[1 - t, :, 0] = V[0, :, t]
+    table = np.array([[1, 0]], dtype=np.int32)
+    out = oracle_mod.gqa_decode_paged(Q, kp, vp, table, np.array([2]), scale)
+    assert np.abs(out[0] - O).max() <= tol
+
+
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_paged_oracle_is_invariant_to_page_placement(oracle_mod, page_size):
+    """Any placement of the pages in the pool, and any content of pages no
+    sequence uses, gives the contiguous result."""
+    w = Workload("pg", 3, 16, 2, 64, 300, "bf16", lens=("list", 300, 1, 129),
+                 seed=5, page_size=page_size)
+    inp = make_inputs(w, pad="nan")
+    a = oracle_mod.gqa_decode_paged(inp["q"], inp["k"], inp["v"],
+                                    inp["block_table"], inp["seq_lens"],
+                                    inp["scale"])
+    b = oracle_mod.gqa_decode(inp["q"], inp["k_contig"], inp["v_contig"],
+                              inp["seq_lens"], inp["scale"])
+    assert np.array_equal(a, b)
+    table = inp["block_table"].numpy()
+    used = set(int(x) for x in table.ravel() if x >= 0)
+    assert len(used) == int(sum((int(L) + page_size - 1) // page_size
+                                for L in inp["seq_lens"]))
