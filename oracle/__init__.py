@@ -69,6 +69,11 @@ def _load():
     lib.oracle_e4m3_to_f64.restype = f64
     lib.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
     lib.oracle_e5m2_to_f64.restype = f64
+    lib.oracle_f32_to_fp8.argtypes = [ctypes.c_float, i32]
+    lib.oracle_f32_to_fp8.restype = ctypes.c_uint8
+    lib.oracle_append_kv.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp,
+                                     i32, i32, i32, i32]
+    lib.oracle_append_kv.restype = i32
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
     _lib = lib
@@ -248,6 +253,36 @@ def gqa_weights(q, k, v, seq_lens, scale, b, h, *, k_scale=None,
     if L < 0:
         raise ValueError("oracle_gqa_weights rejected its arguments")
     return w[:L].copy(), row
+
+
+def f32_to_fp8(v: float, kind: int) -> int:
+    """The oracle's fp32 -> 8-bit code (E4M3 or E5M2), RNE, clamped."""
+    return int(_load().oracle_f32_to_fp8(float(v), int(kind)))
+
+
+def append_kv(k_new, v_new, k_cache, v_cache, seq_lens, *, k_scale=None,
+              v_scale=None):
+    """One cache append on host copies: returns (k_cache, v_cache, k_scale,
+    v_scale, seq_lens, flags) after writing the new rows.  k_new / v_new
+    [B, Hkv, D] float16 / bfloat16; caches [B, Hkv, Smax, D] in the same
+    16-bit type or FP8 E4M3 / E5M2 (then k_scale / v_scale [B, Hkv] fp32)."""
+    import torch
+    lib = _load()
+    kn, it = _as_raw(k_new, "k_new")
+    vn, _ = _as_raw(v_new, "v_new")
+    kc, ct = _as_raw(k_cache.clone(), "k_cache")
+    vc, _ = _as_raw(v_cache.clone(), "v_cache")
+    kc, vc = kc.copy(), vc.copy()
+    B, Hkv, Smax, D = kc.shape
+    lens = np.ascontiguousarray(_lens(seq_lens).copy())
+    ks = vs = None
+    if k_scale is not None:
+        ks = np.ascontiguousarray(k_scale.numpy().astype(np.float32).copy())
+        vs = np.ascontiguousarray(v_scale.numpy().astype(np.float32).copy())
+    flags = lib.oracle_append_kv(_ptr(kn), _ptr(vn), it, _ptr(kc), _ptr(vc),
+                                 ct, _ptr(ks), _ptr(vs), _ptr(lens), B, Hkv,
+                                 Smax, D)
+    return kc, vc, ks, vs, lens, int(flags)
 
 
 def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,

@@ -301,6 +301,116 @@ int oracle_gqa_weights(const void* q, int q_dtype, const void* k,
   return L;
 }
 
+/* ------------------------------------------ cache append (+ FP8 quantise) */
+
+/* Largest finite value of an 8-bit code type. */
+static float fp8_max(int dtype) { return dtype == ORC_E5M2 ? 57344.0f : 448.0f; }
+
+/* fp32 -> 8-bit code, round to nearest even on the format's grid, values
+ * beyond the largest finite value clamped to it ("satfinite").  Written from
+ * the OCP FP8 E4M3 (bias 7, 3 fraction bits, no inf, S.1111.111 NaN) and
+ * E5M2 (bias 15, 2 fraction bits, exponent 31 inf/NaN) layouts. */
+uint8_t oracle_f32_to_fp8(float v, int dtype) {
+  const int mbits = dtype == ORC_E5M2 ? 2 : 3;
+  const int bias = dtype == ORC_E5M2 ? 15 : 7;
+  const int emax = dtype == ORC_E5M2 ? 15 : 8; /* largest unbiased exponent */
+  const double maxv = fp8_max(dtype);
+  const uint8_t maxcode = dtype == ORC_E5M2 ? 0x7B : 0x7E;
+  if (v != v) return 0x7F; /* NaN */
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  double a = fabs((double)v);
+  if (a >= maxv) return sign | maxcode;
+  const double min_normal = ldexp(1.0, 1 - bias);
+  if (a < min_normal) {
+    /* subnormal grid: multiples of 2^(1 - bias - mbits) */
+    double q = nearbyint(a / ldexp(1.0, 1 - bias - mbits));
+    return sign | (uint8_t)q; /* q == 2^mbits is the smallest normal code */
+  }
+  int e;
+  frexp(a, &e);
+  e -= 1; /* a = 1.f * 2^e */
+  double r = nearbyint((a / ldexp(1.0, e) - 1.0) * (double)(1 << mbits));
+  if (r == (double)(1 << mbits)) {
+    r = 0.0;
+    e += 1;
+  }
+  if (e > emax || (dtype != ORC_E5M2 && e == emax && (int)r == 7))
+    return sign | maxcode;
+  return sign | (uint8_t)(((e + bias) << mbits) | (int)r);
+}
+
+/* Appends one token's K and V rows per (sequence, KV head) at position
+ * L_b = seq_lens[b] and sets seq_lens[b] = L_b + 1 ("Grouped Query Attention
+ * (GQA): Efficient Multi-Head Attention", The bottleneck: the cache grows by
+ * one token's K and V per decoding step).  16-bit caches: the rows are copied.
+ * 8-bit caches ("Grouped-Query Attention: How Sharing KV Heads Shrinks
+ * Inference Memory", FP8 KV cache: codes with scaling factors), per (b, kvh)
+ * and tensor, all decisions in fp32:
+ *   a = max_d |x_d|;
+ *   scale s <= 0 (unset): s' = a / MAX (1 if a == 0), earlier codes kept;
+ *   else s' = s doubled until a / s' <= MAX; if it grew, every earlier code
+ *        c of the slab becomes encode(decode(c) * (s / s'));
+ *   the new row's codes are encode(x_d / s'); the scale becomes s'.
+ * A sequence with L_b >= Smax is left unchanged and flags bit 2 (cache full).
+ * Returns the flags (0 when every sequence was appended). */
+int oracle_append_kv(const void* k_new, const void* v_new, int in_dtype,
+                     void* k_cache, void* v_cache, int cache_dtype,
+                     float* k_scale, float* v_scale, int32_t* seq_lens, int B,
+                     int Hkv, int Smax, int D) {
+  int flags = 0;
+  const int fp8 = cache_dtype == ORC_E4M3 || cache_dtype == ORC_E5M2;
+  const float M = fp8 ? fp8_max(cache_dtype) : 0.0f;
+  for (int b = 0; b < B; ++b) {
+    int L = seq_lens[b] < 0 ? 0 : seq_lens[b];
+    if (L >= Smax) {
+      flags |= 4;
+      continue;
+    }
+    for (int j = 0; j < Hkv; ++j) {
+      for (int which = 0; which < 2; ++which) {
+        const void* src = which ? v_new : k_new;
+        void* cache = which ? v_cache : k_cache;
+        float* scales = which ? v_scale : k_scale;
+        const size_t row = (size_t)b * Hkv + j;
+        const size_t slab = row * (size_t)Smax * D;
+        if (!fp8) {
+          for (int d = 0; d < D; ++d)
+            ((uint16_t*)cache)[slab + (size_t)L * D + d] =
+                ((const uint16_t*)src)[row * D + d];
+          continue;
+        }
+        uint8_t* codes = (uint8_t*)cache;
+        float a = 0.0f;
+        for (int d = 0; d < D; ++d) {
+          float x = (float)load_elem(src, row * D + d, in_dtype);
+          if (fabsf(x) > a) a = fabsf(x);
+        }
+        float s = scales[row], s2;
+        if (!(s > 0.0f)) {
+          s2 = a > 0.0f ? a / M : 1.0f;
+        } else {
+          s2 = s;
+          for (int it = 0; it < 256 && a / s2 > M; ++it) s2 = s2 * 2.0f;
+          if (s2 != s) {
+            const float ratio = s / s2;
+            for (size_t i = 0; i < (size_t)L * D; ++i) {
+              float c = (float)load_elem(codes, slab + i, cache_dtype);
+              codes[slab + i] = oracle_f32_to_fp8(c * ratio, cache_dtype);
+            }
+          }
+        }
+        for (int d = 0; d < D; ++d) {
+          float x = (float)load_elem(src, row * D + d, in_dtype);
+          codes[slab + (size_t)L * D + d] = oracle_f32_to_fp8(x / s2, cache_dtype);
+        }
+        scales[row] = s2;
+      }
+    }
+    seq_lens[b] = L + 1;
+  }
+  return flags;
+}
+
 /* Number of threads the oracle would use by default. */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -423,3 +423,117 @@ def test_paged_oracle_is_invariant_to_page_placement(oracle_mod, page_size):
     used = set(int(x) for x in table.ravel() if x >= 0)
     assert len(used) == int(sum((int(L) + page_size - 1) // page_size
                                 for L in inp["seq_lens"]))
+
+
+# ------------------------------------------ FP8 encoder (cache append step)
+
+@pytest.mark.parametrize("kind,dtype,maxv", [
+    (2, torch.float8_e4m3fn, 448.0), (4, torch.float8_e5m2, 57344.0)])
+def test_fp8_encoder_matches_torch_in_range(oracle_mod, kind, dtype, maxv):
+    """Round-to-nearest-even onto the 8-bit grid, checked against torch's
+    cast on every finite code, every midpoint between neighbouring codes
+    (the ties), random values and subnormals, all within the finite range."""
+    rng = np.random.default_rng(kind)
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(dtype)
+    vals = codes.float()
+    vals = vals[torch.isfinite(vals) & (vals.abs() <= maxv)]
+    s = torch.sort(vals).values
+    x = torch.cat([vals, (s[1:] + s[:-1]) / 2,
+                   torch.tensor(rng.uniform(-maxv, maxv, 4000),
+                                dtype=torch.float32),
+                   torch.tensor(rng.uniform(-0.01, 0.01, 4000),
+                                dtype=torch.float32)])
+    ref = x.to(dtype).view(torch.uint8).numpy()
+    ours = np.array([oracle_mod.f32_to_fp8(v, kind) for v in x.tolist()],
+                    dtype=np.uint8)
+    assert np.array_equal(ref, ours)
+
+
+def test_fp8_encoder_clamps_beyond_the_largest_value(oracle_mod):
+    assert oracle_mod.f32_to_fp8(1e6, 2) == 0x7E       # +448
+    assert oracle_mod.f32_to_fp8(-500.0, 2) == 0xFE    # -448
+    assert oracle_mod.f32_to_fp8(1e9, 4) == 0x7B       # +57344
+    assert oracle_mod.f32_to_fp8(-70000.0, 4) == 0xFB
+
+
+# ------------------------------------------------- cache append (the oracle)
+
+def _append_case(cache_kind, seed, B=3, Hkv=2, Smax=40, D=64, lens=(5, 0, 39),
+                 scale_mul=None):
+    """Random caches with lens[b] valid tokens, new rows, and scales."""
+    g = torch.Generator().manual_seed(seed)
+    kn = torch.randn((B, Hkv, D), generator=g).to(torch.bfloat16)
+    vn = (3.0 * torch.randn((B, Hkv, D), generator=g)).to(torch.bfloat16)
+    seq = torch.tensor(lens, dtype=torch.int32)
+    if cache_kind == "bf16":
+        kc = torch.randn((B, Hkv, Smax, D), generator=g).to(torch.bfloat16)
+        vc = torch.randn((B, Hkv, Smax, D), generator=g).to(torch.bfloat16)
+        return kn, vn, kc, vc, seq, None, None
+    dt = torch.float8_e4m3fn if cache_kind == "e4m3" else torch.float8_e5m2
+    kc = torch.randn((B, Hkv, Smax, D), generator=g).mul(50).to(dt)
+    vc = torch.randn((B, Hkv, Smax, D), generator=g).mul(50).to(dt)
+    ks = torch.rand((B, Hkv), generator=g).add(0.5).mul(scale_mul)
+    vs = torch.rand((B, Hkv), generator=g).add(0.5).mul(scale_mul)
+    return kn, vn, kc, vc, seq, ks.float(), vs.float()
+
+
+def test_append_16bit_copies_the_row(oracle_mod):
+    kn, vn, kc, vc, seq, _, _ = _append_case("bf16", 1)
+    k2, v2, _, _, lens, flags = oracle_mod.append_kv(kn, vn, kc, vc, seq)
+    assert flags == 0 and list(lens) == [6, 1, 40]
+    k2 = torch.from_numpy(k2).view(torch.bfloat16)
+    v2 = torch.from_numpy(v2).view(torch.bfloat16)
+    for b, L in enumerate(seq.tolist()):
+        assert torch.equal(k2[b, :, L], kn[b])
+        assert torch.equal(v2[b, :, L], vn[b])
+        mask = torch.ones(k2.shape[2], dtype=torch.bool)
+        mask[L] = False
+        assert torch.equal(k2[b, :, mask], kc[b, :, mask])
+
+
+@pytest.mark.parametrize("kind", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("scale_mul", [10.0, 1e-5, 0.0])
+def test_append_fp8_quantise_and_rescale(oracle_mod, kind, scale_mul):
+    """Against float32 arithmetic and torch's casts: the scale (kept,
+    doubled until the new row fits, or set from the row when unset), the
+    re-encoded earlier codes and the new row's codes."""
+    dt = torch.float8_e4m3fn if kind == "e4m3" else torch.float8_e5m2
+    M = np.float32(448.0 if kind == "e4m3" else 57344.0)
+    kn, vn, kc, vc, seq, ks, vs = _append_case(kind, 2, scale_mul=scale_mul)
+    k2, v2, ks2, vs2, lens, flags = oracle_mod.append_kv(
+        kn, vn, kc, vc, seq, k_scale=ks, v_scale=vs)
+    assert flags == 0 and list(lens) == [6, 1, 40]
+    for new, old, sc, got, sc2 in ((kn, kc, ks, k2, ks2), (vn, vc, vs, v2, vs2)):
+        got = torch.from_numpy(got).view(dt)
+        for b, L in enumerate(seq.tolist()):
+            for j in range(new.shape[1]):
+                x = new[b, j].float().numpy()
+                a = np.float32(np.abs(x).max())
+                s = np.float32(sc[b, j])
+                if not s > 0:
+                    s2 = np.float32(a / M) if a > 0 else np.float32(1.0)
+                    prev = old[b, j, :L]
+                else:
+                    s2 = s
+                    while np.float32(a / s2) > M:
+                        s2 = np.float32(s2 * np.float32(2.0))
+                    ratio = np.float32(s / s2)
+                    prev = (old[b, j, :L].float() *
+                            torch.tensor(ratio)).to(dt) if s2 != s \
+                        else old[b, j, :L]
+                assert np.float32(sc2[b, j]) == s2
+                assert torch.equal(got[b, j, :L].view(torch.uint8),
+                                   prev.view(torch.uint8))
+                row = (torch.from_numpy(x) / torch.tensor(s2)).to(dt)
+                assert torch.equal(got[b, j, L].view(torch.uint8),
+                                   row.view(torch.uint8))
+                if scale_mul == 1e-5:
+                    assert s2 > s          # the tiny scales had to grow
+
+
+def test_append_full_cache_is_flagged_and_left_alone(oracle_mod):
+    kn, vn, kc, vc, seq, _, _ = _append_case("bf16", 3, lens=(40, 2, -3))
+    k2, _, _, _, lens, flags = oracle_mod.append_kv(kn, vn, kc, vc, seq)
+    assert flags == 4
+    assert list(lens) == [40, 3, 1]      # full, appended, negative as 0
+    assert torch.equal(torch.from_numpy(k2).view(torch.bfloat16)[0], kc[0])
