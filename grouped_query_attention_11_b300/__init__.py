@@ -13,6 +13,8 @@ its names:
   KV head) scales;
 * :func:`gqa_decode_paged` — the same over a paged cache (page pool + block
   table);
+* :func:`gqa_append_kv` — the step before: write the new token's K/V (FP8
+  quantised with per-(sequence, KV head) scales) and bump seq_lens;
 * :func:`gqa_decode_static` — gqa_decode with a fixed scratch array instead of
   any device allocation;
 * :func:`gqa_kv_bytes_per_token`, :func:`gqa_status_string`,
@@ -39,6 +41,8 @@ SIGNATURES = {
                           _I32, _I32, _I32, _VP]),
     "gqa_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
                               _I32, _I32, _I32, _I32, _I32, _I32, _VP]),
+    "gqa_append_kv": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32,
+                             _I32, _I32, _I32, _I32, _VP]),
     "gqa_decode_paged": (_I32, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
                                 _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                 _VP]),
@@ -170,6 +174,43 @@ def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out=None,
     if st != GQA_OK:
         raise GQAError(st, "gqa_decode")
     return out
+
+
+def gqa_append_kv(k_new, v_new, k_cache, v_cache, seq_lens, k_scale=None,
+                  v_scale=None, stream=None):
+    """Writes the new token's K/V rows [B, Hkv, D] at position seq_lens[b] of
+    each sequence's cache [B, Hkv, Smax, D] and increments seq_lens (int32).
+    16-bit caches take the rows as they are; float8_e4m3fn / float8_e5m2
+    caches quantise them with k_scale / v_scale [B, Hkv] float32, which are
+    updated (grown by powers of two, re-encoding earlier codes) in place."""
+    import torch
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
+                 ("v_cache", v_cache), ("seq_lens", seq_lens)):
+        _check_dev(n, t)
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    if v_new.dtype != k_new.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("K and V must share their dtypes")
+    in_code = _dtype_code(k_new)
+    if k_cache.dtype in (torch.float16, torch.bfloat16):
+        cache_code = _dtype_code(k_cache)
+        ks = vs = 0
+    else:
+        cache_code = _fp8_code(k_cache)
+        for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if t is None:
+                raise ValueError(f"{n} is required for an 8-bit cache")
+            _check_dev(n, t)
+            if t.dtype != torch.float32:
+                raise TypeError(f"{n} must be float32")
+        ks, vs = k_scale.data_ptr(), v_scale.data_ptr()
+    B, Hkv, Smax, D = k_cache.shape
+    st = lib().gqa_append_kv(k_new.data_ptr(), v_new.data_ptr(),
+                             k_cache.data_ptr(), v_cache.data_ptr(), ks, vs,
+                             seq_lens.data_ptr(), B, Hkv, Smax, D, in_code,
+                             cache_code, _stream_handle(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_append_kv")
 
 
 def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens,

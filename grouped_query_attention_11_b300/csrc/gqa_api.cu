@@ -13,6 +13,7 @@
 #include <utility>
 
 #include "gqa.h"
+#include "gqa_append_kernel.cuh"
 #include "gqa_decode_kernel.cuh"
 
 namespace gqa {
@@ -549,6 +550,65 @@ gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
 void gqa_set_num_ctas(int num_ctas) {
   std::lock_guard<std::mutex> lock(gqa::g_mu);
   gqa::g_num_ctas_override = num_ctas > 0 ? num_ctas : 0;
+}
+
+gqa_status gqa_append_kv(const void* k_new, const void* v_new, void* k_cache,
+                         void* v_cache, float* k_scale, float* v_scale,
+                         int32_t* seq_lens, int B, int Hkv, int Smax, int D,
+                         gqa_dtype in_dtype, gqa_dtype cache_dtype,
+                         void* stream_ptr) {
+  using namespace gqa;
+  t_last_launches = 0;
+  if (in_dtype != GQA_F16 && in_dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  const bool fp8 = cache_dtype == GQA_E4M3 || cache_dtype == GQA_E5M2;
+  if (!fp8 && cache_dtype != in_dtype) return GQA_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !k_cache || !v_cache || !seq_lens)
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(seq_lens, 4))
+    return GQA_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale || !aligned(k_scale, 4) ||
+              !aligned(v_scale, 4)))
+    return GQA_ERR_INVALID_ARG;
+  if (B < 1 || Hkv < 1 || Smax < 1) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+  try {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+    Scratch* sc = nullptr;  // only its error word is used
+    if (scratch_for(dev, stream, 1, 1, &sc) != cudaSuccess) return GQA_ERR_CUDA;
+    AppendParams p = {};
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.seq_lens = seq_lens;
+    p.error = static_cast<uint32_t*>(sc->ctl);
+    p.B = B;
+    p.Hkv = Hkv;
+    p.Smax = Smax;
+    p.D = D;
+    const bool bf16 = in_dtype == GQA_BF16;
+    void (*fn)(const AppendParams) =
+        cache_dtype == GQA_E4M3
+            ? (bf16 ? gqa_append_kernel<true, kKvE4M3>
+                    : gqa_append_kernel<false, kKvE4M3>)
+        : cache_dtype == GQA_E5M2
+            ? (bf16 ? gqa_append_kernel<true, kKvE5M2>
+                    : gqa_append_kernel<false, kKvE5M2>)
+            : (bf16 ? gqa_append_kernel<true, kKvBF16>
+                    : gqa_append_kernel<false, kKvF16>);
+    fn<<<B, kAppendThreads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    t_last_launches = 1;
+    return GQA_OK;
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
 }
 
 gqa_status gqa_decode_paged(const void* q, const void* k_pages,

@@ -103,6 +103,7 @@ __host__ __device__ constexpr bool is_fp8(int kv) {
 enum ErrorBits : uint32_t {
   kErrWaitTimeout = 1u,  // a pipeline wait gave up after its time limit
   kErrBadPage = 2u,      // a block-table entry outside [0, num_pages)
+  kErrCacheFull = 4u,    // an append found a sequence's cache full
 };
 
 struct DecodeParams {

@@ -121,6 +121,42 @@ gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
                           gqa_dtype qo_dtype, void* stream);
 
 /*
+ * gqa_append_kv — the step before the decode: writes the new token's K and V
+ * rows of every KV head into the cache at position L_b = seq_lens[b] and sets
+ * seq_lens[b] = L_b + 1 ("Grouped Query Attention (GQA): Efficient Multi-Head
+ * Attention", The bottleneck: the cache grows by one token per step).
+ *
+ *   k_new, v_new     [B, Hkv, D] in_dtype (GQA_F16 / GQA_BF16), device,
+ *                    16-byte aligned
+ *   k_cache, v_cache [B, Hkv, Smax, D] cache_dtype, device, 16-byte aligned:
+ *                    in_dtype (rows copied as they are), or GQA_E4M3 /
+ *                    GQA_E5M2 (rows quantised)
+ *   k_scale, v_scale [B, Hkv] fp32, device, read and updated (8-bit caches
+ *                    only; may be NULL otherwise)
+ *   seq_lens         [B] int32, device, read and incremented
+ *   D in {64, 128}
+ *
+ * 8-bit caches ("Grouped-Query Attention: How Sharing KV Heads Shrinks
+ * Inference Memory", FP8 KV cache: scaling factors) decide every code in fp32
+ * (IEEE division, round to nearest even, clamped to the format's largest
+ * value), per (sequence, KV head) and tensor: with a = max |x| of the new
+ * row, an unset scale (<= 0) becomes a / MAX (1 if a == 0; earlier codes are
+ * left as they are); otherwise the scale doubles until a / scale <= MAX and,
+ * if it grew, the earlier codes are re-encoded with the power-of-two ratio
+ * old / new (exact except below the format's normal range); the new codes
+ * are x / scale.  MAX is 448 (E4M3) or 57344 (E5M2).
+ *
+ * A sequence with seq_lens[b] >= Smax is left unchanged and sets bit 2 of
+ * gqa_device_errors; a negative length counts as 0.  Asynchronous on
+ * `stream`; one kernel.
+ */
+gqa_status gqa_append_kv(const void* k_new, const void* v_new, void* k_cache,
+                         void* v_cache, float* k_scale, float* v_scale,
+                         int32_t* seq_lens, int B, int Hkv, int Smax, int D,
+                         gqa_dtype in_dtype, gqa_dtype cache_dtype,
+                         void* stream);
+
+/*
  * gqa_decode_paged — gqa_decode over a paged KV cache: the cache lives in a
  * pool of fixed-size pages and a block table maps each sequence's token
  * ranges to pages ("Grouped-Query Attention: How Sharing KV Heads Shrinks
@@ -206,7 +242,7 @@ const char* gqa_status_string(gqa_status status);
  * fault flags the kernels raised on it since the last query: 0 when none.
  * Bit 0: a pipeline wait gave up after its time limit (the affected outputs
  * are unspecified).  Bit 1: a paged call met a block-table entry outside
- * [0, num_pages).  Returns GQA_ERR_CUDA if the synchronisation fails.
+ * [0, num_pages).  Bit 2: an append found a sequence's cache full.  Returns GQA_ERR_CUDA if the synchronisation fails.
  */
 gqa_status gqa_device_errors(void* stream, uint32_t* flags);
 

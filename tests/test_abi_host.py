@@ -141,3 +141,24 @@ def test_decode_paged_rejects_invalid_arguments(L, kw):
                                 dict(D=96)])
 def test_decode_paged_unsupported(L, kw):
     assert _callp(**kw) == gq.GQA_ERR_UNSUPPORTED
+
+
+def _calla(kn=A, vn=A * 2, kc=A * 3, vc=A * 4, ks=A * 6, vs=A * 7, lens=A * 5,
+           B=2, Hkv=2, Smax=64, D=64, ind=gq.GQA_BF16, cd=gq.GQA_E4M3):
+    return gq.lib().gqa_append_kv(kn, vn, kc, vc, ks, vs, lens, B, Hkv, Smax,
+                                  D, ind, cd, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(kn=None), dict(vc=None), dict(lens=None), dict(kn=A + 8),
+    dict(lens=A * 5 + 2), dict(ks=None), dict(vs=A * 7 + 1), dict(B=0),
+    dict(Hkv=0), dict(Smax=0), dict(ind=gq.GQA_E4M3),
+    dict(ind=gq.GQA_F16, cd=gq.GQA_BF16), dict(cd=9),
+])
+def test_append_rejects_invalid_arguments(L, kw):
+    assert _calla(**kw) == gq.GQA_ERR_INVALID_ARG
+    assert gq.gqa_last_launch_count() == 0
+
+
+def test_append_unsupported_head_dim(L):
+    assert _calla(D=96) == gq.GQA_ERR_UNSUPPORTED
