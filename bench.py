@@ -190,6 +190,82 @@ def cpu_baseline(w, inp, budget_s: float = 10.0):
 
 # ------------------------------------------------------------------ runner
 
+def bench_append(a, w, name, peak, peak_kind):
+    """K back-to-back gqa_append_kv calls on the workload's shape (1 GPU):
+    every call appends one token to every sequence, from a length that
+    leaves room for all of them.  FP8 scales start at 1 (N(0,1) rows fit, so
+    no earlier code is re-encoded: the common step)."""
+    import torch
+    import grouped_query_attention_11_b300 as gq
+    dev = torch.device("cuda", torch.cuda.current_device())
+    K, warmup = a.steps, max(3, a.warmup)
+    start_len = max(0, w.Smax - K - warmup - 2)
+    g = torch.Generator().manual_seed(w.seed)
+    qdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+    cdt = {"same": qdt, "e4m3": torch.float8_e4m3fn,
+           "e5m2": torch.float8_e5m2}[w.kv]
+    kn = torch.randn((w.B, w.Hkv, w.D), generator=g).to(qdt).to(dev)
+    vn = torch.randn((w.B, w.Hkv, w.D), generator=g).to(qdt).to(dev)
+    shape = (w.B, w.Hkv, w.Smax, w.D)
+    kc = torch.zeros(shape, dtype=torch.uint8 if w.kv != "same" else qdt,
+                     device=dev)
+    vc = torch.zeros_like(kc)
+    if w.kv != "same":
+        kc, vc = kc.view(cdt), vc.view(cdt)
+        ks = torch.ones((w.B, w.Hkv), dtype=torch.float32, device=dev)
+        vs = torch.ones_like(ks)
+    else:
+        ks = vs = None
+    lens = torch.full((w.B,), start_len, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gq.gqa_append_kv(kn, vn, kc, vc, lens, k_scale=ks, v_scale=vs,
+                         stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3 if sampler.proc else 0)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    launches = 0
+    for _ in range(K):
+        step()
+        launches += gq.gqa_last_launch_count()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    assert gq.gqa_device_errors(stream) == 0
+    assert int(lens[0]) == start_len + K + warmup
+    us = ev0.elapsed_time(ev1) * 1e3 / K
+    eb = 1 if w.kv != "same" else 2
+    # bytes per append: new rows read (16-bit) + cache rows written + lens
+    algo = 2 * w.B * w.Hkv * w.D * (2 + eb) + 8 * w.B + (
+        16 * w.B * w.Hkv if w.kv != "same" else 0)
+    achieved = algo / (us * 1e-6) / 1e9
+    line = {"metric": "GQA cache append us/step (1 GPU)", "value": us,
+            "unit": "us/step", "n_gpus": 1, "steps": K, "warmup": warmup,
+            "ms_per_step": us / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype if w.kv == "same" else
+            f"{w.kv} KV / {w.dtype} rows", "data": "synthetic",
+            "config": {"workload": name, "op": "append", "B": w.B,
+                       "Hkv": w.Hkv, "D": w.D, "Smax": w.Smax,
+                       "start_len": start_len},
+            "algorithmic_bytes_per_step": algo,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": None,
+                         "note": "a few KB per call: launch-latency bound"},
+            "gpu_launches": launches, "clocks": sampler.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -206,6 +282,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--op", default="decode", choices=["decode", "append"],
+                    help="decode: the decode step (default); append: the "
+                         "cache-append step before it")
     a = ap.parse_args(argv)
 
     from grouped_query_attention_11_b300.workloads import (HEADLINE,
@@ -251,6 +330,9 @@ def main(argv=None):
 
     import torch
     import grouped_query_attention_11_b300 as gq
+
+    if a.op == "append":
+        return bench_append(a, w, name, peak, peak_kind)
 
     if ws > 1:
         import torch.distributed as dist

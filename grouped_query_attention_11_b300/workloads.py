@@ -63,6 +63,7 @@ class Workload:
                                  # ("list", l0, l1, ...)
     seed: int = 1000
     page_size: int = 0           # > 0: paged cache with pages of this size
+    T: int = 1                   # new tokens per sequence (> 1: q [B,Hq,T,D])
 
     @property
     def G(self) -> int:
@@ -80,7 +81,7 @@ class Workload:
         """K+V bytes of the valid tokens + q + out (+ FP8 scales)."""
         total_tokens = int(sum(int(x) for x in seq_lens))
         kv = 2 * self.Hkv * self.D * self.kv_elem_bytes * total_tokens
-        qo = 2 * self.B * self.Hq * self.D * 2
+        qo = 2 * self.B * self.Hq * self.T * self.D * 2
         sc = 2 * self.B * self.Hkv * 4 if self.kv in _FP8 else 0
         return kv + qo + sc
 
@@ -166,7 +167,8 @@ def make_inputs(w: Workload, *, pad: str = "nan",
     if w.B > 0 and int(seq_lens.max()) > w.Smax:
         raise ValueError("a sequence is longer than the cache")
     qdt = _DT[w.dtype]
-    q = torch.randn((w.B, w.Hq, w.D), generator=gen).to(qdt)
+    qshape = (w.B, w.Hq, w.D) if w.T == 1 else (w.B, w.Hq, w.T, w.D)
+    q = torch.randn(qshape, generator=gen).to(qdt)
 
     fp8 = w.kv in _FP8
     if fp8:

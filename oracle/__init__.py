@@ -69,6 +69,10 @@ def _load():
     lib.oracle_e4m3_to_f64.restype = f64
     lib.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
     lib.oracle_e5m2_to_f64.restype = f64
+    lib.oracle_gqa_decode_chunk.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp,
+                                            f64, vp, i32, i32, i32, i32, i32,
+                                            i32, i32]
+    lib.oracle_gqa_decode_chunk.restype = i32
     lib.oracle_f32_to_fp8.argtypes = [ctypes.c_float, i32]
     lib.oracle_f32_to_fp8.restype = ctypes.c_uint8
     lib.oracle_append_kv.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp,
@@ -167,6 +171,33 @@ def gqa_decode(q, k, v, seq_lens, scale, *, k_scale=None, v_scale=None,
                                B, Hq, Hkv, Smax, D, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gqa_decode rejected its arguments")
+    return out
+
+
+def gqa_decode_chunk(q, k, v, seq_lens, scale, *, k_scale=None,
+                     v_scale=None, nthreads: int = 0) -> np.ndarray:
+    """out[B, Hq, T, D] (float64) for T new tokens per sequence (the last T
+    of its seq_lens[b] cached tokens), each attending causally: token i sees
+    cached tokens t <= seq_lens[b] - T + i.  q: [B, Hq, T, D]."""
+    lib = _load()
+    qa, qt = _as_raw(q, "q")
+    ka, kt = _as_raw(k, "k")
+    va, vt = _as_raw(v, "v")
+    if kt != vt:
+        raise ValueError("k and v must share an element type")
+    B, Hq, T, D = qa.shape
+    _, Hkv, Smax, D2 = ka.shape
+    if D2 != D or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    lens = _lens(seq_lens)
+    ks, vs = _scales(k_scale), _scales(v_scale)
+    out = np.zeros((B, Hq, T, D), dtype=np.float64)
+    rc = lib.oracle_gqa_decode_chunk(_ptr(qa), qt, _ptr(ka), _ptr(va), kt,
+                                     _ptr(ks), _ptr(vs), _ptr(lens),
+                                     float(scale), _ptr(out), B, Hq, Hkv, T,
+                                     Smax, D, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gqa_decode_chunk rejected its arguments")
     return out
 
 

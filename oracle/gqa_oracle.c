@@ -157,27 +157,21 @@ typedef struct {
   int q_dtype, kv_dtype;
 } orc_problem;
 
-/* Computes out[0..D) for query head h of sequence b.  If w is non-NULL it
- * receives the L softmax weights.  `scores` is caller scratch of Smax doubles.
- * Returns the number of valid tokens L used. */
-static int attend_row(const orc_problem* p, int b, int h, double* out,
-                      double* w, double* scores) {
-  const int G = p->Hq / p->Hkv;   /* query heads per KV head */
-  const int kvh = h / G;          /* contiguous grouping */
-  int L = p->seq_lens[b];
-  if (L < 0) L = 0;
-  if (L > p->Smax) L = p->Smax;
-
-  const size_t q_off = ((size_t)b * p->Hq + h) * p->D;
+/* Attention of one query row against the first n cached tokens of KV head
+ * kvh of sequence b: the query is D elements at q_off of the query tensor.
+ * If w is non-NULL it receives the n softmax weights.  `scores` is caller
+ * scratch of Smax doubles.  Returns n. */
+static int attend(const orc_problem* p, int b, int kvh, size_t q_off, int n,
+                  double* out, double* w, double* scores) {
   const size_t kv_off = ((size_t)b * p->Hkv + kvh) * (size_t)p->Smax * p->D;
   const double ks = p->k_scale ? p->k_scale[b * p->Hkv + kvh] : 1.0;
   const double vs = p->v_scale ? p->v_scale[b * p->Hkv + kvh] : 1.0;
 
   for (int d = 0; d < p->D; ++d) out[d] = 0.0;
-  if (L == 0) return 0;
+  if (n <= 0) return 0;
 
   /* scores: s_t = scale * sum_d q_d * k_{t,d} */
-  for (int t = 0; t < L; ++t) {
+  for (int t = 0; t < n; ++t) {
     double dot = 0.0;
     for (int d = 0; d < p->D; ++d) {
       double qd = load_elem(p->q, q_off + d, p->q_dtype);
@@ -189,26 +183,43 @@ static int attend_row(const orc_problem* p, int b, int h, double* out,
 
   /* softmax with the row maximum subtracted */
   double m = scores[0];
-  for (int t = 1; t < L; ++t)
+  for (int t = 1; t < n; ++t)
     if (scores[t] > m) m = scores[t];
   double z = 0.0;
-  for (int t = 0; t < L; ++t) {
+  for (int t = 0; t < n; ++t) {
     scores[t] = exp(scores[t] - m);
     z += scores[t];
   }
-  for (int t = 0; t < L; ++t) scores[t] /= z;
+  for (int t = 0; t < n; ++t) scores[t] /= z;
   if (w)
-    for (int t = 0; t < L; ++t) w[t] = scores[t];
+    for (int t = 0; t < n; ++t) w[t] = scores[t];
 
   /* output: sum_t w_t * v_t */
-  for (int t = 0; t < L; ++t) {
+  for (int t = 0; t < n; ++t) {
     const double wt = scores[t];
     for (int d = 0; d < p->D; ++d) {
       double vd = load_elem(p->v, kv_off + (size_t)t * p->D + d, p->kv_dtype) * vs;
       out[d] += wt * vd;
     }
   }
+  return n;
+}
+
+static int clamped_len(const orc_problem* p, int b) {
+  int L = p->seq_lens[b];
+  if (L < 0) L = 0;
+  if (L > p->Smax) L = p->Smax;
   return L;
+}
+
+/* Computes out[0..D) for query head h of sequence b (one new token, q
+ * [B, Hq, D]): attention over all L_b cached tokens of KV head floor(h/G). */
+static int attend_row(const orc_problem* p, int b, int h, double* out,
+                      double* w, double* scores) {
+  const int G = p->Hq / p->Hkv;   /* query heads per KV head */
+  const int kvh = h / G;          /* contiguous grouping */
+  const size_t q_off = ((size_t)b * p->Hq + h) * p->D;
+  return attend(p, b, kvh, q_off, clamped_len(p, b), out, w, scores);
 }
 
 static int check_problem(const orc_problem* p) {
@@ -299,6 +310,48 @@ int oracle_gqa_weights(const void* q, int q_dtype, const void* k,
   int L = attend_row(&p, b, h, out_row, w, scores);
   free(scores);
   return L;
+}
+
+/* Multi-token step (chunked prefill / speculative decode): q and out are
+ * [B, Hq, T, D]; the last T of sequence b's L_b cached tokens are the new
+ * ones, and new token i (0-based) attends causally to cached tokens
+ * t <= L_b - T + i, i.e. to the first max(0, L_b - T + i + 1) of them
+ * (scaled dot-product attention with a causal mask, as in "Grouped Query
+ * Attention: Why 8 KV Heads Decide Your Batch Size", The repeat_kv trap:
+ * scaled_dot_product_attention(..., is_causal=True, enable_gqa=True)).
+ * T = 1 is the decode step.  Returns 0 on success. */
+int oracle_gqa_decode_chunk(const void* q, int q_dtype, const void* k,
+                            const void* v, int kv_dtype, const double* k_scale,
+                            const double* v_scale, const int32_t* seq_lens,
+                            double scale, double* out, int B, int Hq, int Hkv,
+                            int T, int Smax, int D, int nthreads) {
+  orc_problem p = {q, k, v, k_scale, v_scale, seq_lens, scale,
+                   B, Hq, Hkv, Smax, D, q_dtype, kv_dtype};
+  if (check_problem(&p) || !out || T < 1) return 1;
+  const long rows = (long)B * Hq * T;
+  const int G = Hq / Hkv;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)Smax);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (long r = 0; r < rows; ++r) {
+      const int b = (int)(r / ((long)Hq * T));
+      const int h = (int)((r / T) % Hq);
+      const int i = (int)(r % T);
+      const int L = clamped_len(&p, b);
+      int n = L - T + i + 1;
+      if (n > L) n = L;
+      attend(&p, b, h / G, (size_t)r * D, n, out + (size_t)r * D, NULL,
+             scores);
+    }
+    free(scores);
+  }
+  return 0;
 }
 
 /* ------------------------------------------ cache append (+ FP8 quantise) */

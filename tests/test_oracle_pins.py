@@ -537,3 +537,56 @@ def test_append_full_cache_is_flagged_and_left_alone(oracle_mod):
     assert flags == 4
     assert list(lens) == [40, 3, 1]      # full, appended, negative as 0
     assert torch.equal(torch.from_numpy(k2).view(torch.bfloat16)[0], kc[0])
+
+
+# ---------------------------------- multi-token causal step (chunk oracle)
+
+def test_chunk_with_one_token_is_the_decode_step(oracle_mod):
+    w = Workload("c1", 3, 16, 4, 64, 90, "bf16", lens=("list", 90, 1, 33),
+                 seed=21)
+    inp = make_inputs(w, pad="nan")
+    a = oracle_mod.gqa_decode(inp["q"], inp["k"], inp["v"], inp["seq_lens"],
+                              inp["scale"])
+    c = oracle_mod.gqa_decode_chunk(inp["q"][:, :, None, :], inp["k"],
+                                    inp["v"], inp["seq_lens"], inp["scale"])
+    assert np.array_equal(a, c[:, :, 0, :])
+
+
+def test_chunk_token_i_is_a_decode_over_its_prefix(oracle_mod):
+    """New token i of a T-token chunk sees exactly the first L - T + i + 1
+    cached tokens: the same as a one-token step with that length."""
+    w = Workload("c4", 2, 16, 2, 128, 200, "f16", lens=("list", 200, 77),
+                 seed=22, T=5)
+    inp = make_inputs(w, pad="nan")
+    c = oracle_mod.gqa_decode_chunk(inp["q"], inp["k"], inp["v"],
+                                    inp["seq_lens"], inp["scale"])
+    for i in range(5):
+        lens_i = inp["seq_lens"] - 5 + i + 1
+        d = oracle_mod.gqa_decode(inp["q"][:, :, i, :].contiguous(), inp["k"],
+                                  inp["v"], lens_i, inp["scale"])
+        assert np.array_equal(c[:, :, i, :], d)
+
+
+def test_chunk_longer_than_the_cache_gives_zero_rows(oracle_mod):
+    w = Workload("c_short", 1, 4, 2, 64, 8, "bf16", lens=("list", 3), seed=23,
+                 T=5)
+    inp = make_inputs(w, pad="nan")
+    c = oracle_mod.gqa_decode_chunk(inp["q"], inp["k"], inp["v"],
+                                    inp["seq_lens"], inp["scale"])
+    assert np.count_nonzero(c[0, :, :2]) == 0     # tokens 0, 1 see nothing
+    assert np.isfinite(c).all() and np.count_nonzero(c[0, :, 2:]) > 0
+
+
+def test_full_causal_prefill_matches_torch_sdpa(oracle_mod):
+    """T = L (the whole cache is new): the causal GQA attention of the
+    pages' SDPA call, scaled_dot_product_attention(q, k, v, is_causal=True,
+    enable_gqa=True), in float64."""
+    for Hq, Hkv in ((8, 2), (4, 4), (8, 1)):
+        w = Workload("pf", 2, Hq, Hkv, 64, 40, "bf16", seed=24 + Hkv, T=40)
+        inp = make_inputs(w, pad="nan")
+        c = oracle_mod.gqa_decode_chunk(inp["q"], inp["k"], inp["v"],
+                                        inp["seq_lens"], inp["scale"])
+        ref = F.scaled_dot_product_attention(
+            inp["q"].double(), inp["k"].double(), inp["v"].double(),
+            scale=inp["scale"], is_causal=True, enable_gqa=True)
+        assert np.abs(c - ref.numpy()).max() <= 1e-12
