@@ -107,7 +107,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
+    def __init__(self, gpu_index: int, period_ms: int = 200):
         self.proc = None
         self.rows = []
         self.gpu_index = gpu_index
@@ -219,9 +219,22 @@ def bench_append(a, w, name, peak, peak_kind):
     lens = torch.full((w.B,), start_len, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
+    # checked once through the public wrapper, then one C-ABI call per step
+    gq.gqa_append_kv(kn, vn, kc, vc, lens, k_scale=ks, v_scale=vs,
+                     stream=stream)
+    torch.cuda.synchronize()
+    lens.fill_(start_len)
+    fn = gq.lib().gqa_append_kv
+    code = {"f16": gq.GQA_F16, "bf16": gq.GQA_BF16}[w.dtype]
+    ccode = {"same": code, "e4m3": gq.GQA_E4M3, "e5m2": gq.GQA_E5M2}[w.kv]
+    args = (kn.data_ptr(), vn.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+            ks.data_ptr() if ks is not None else None,
+            vs.data_ptr() if vs is not None else None, lens.data_ptr(), w.B,
+            w.Hkv, w.Smax, w.D, code, ccode, stream.cuda_stream)
+
     def step():
-        gq.gqa_append_kv(kn, vn, kc, vc, lens, k_scale=ks, v_scale=vs,
-                         stream=stream)
+        if fn(*args) != gq.GQA_OK:
+            raise RuntimeError("gqa_append_kv failed")
 
     for _ in range(warmup):
         step()

@@ -13,6 +13,8 @@ its names:
   KV head) scales;
 * :func:`gqa_decode_paged` — the same over a paged cache (page pool + block
   table);
+* :func:`gqa_decode_chunk` — T new tokens per sequence, causal within the
+  chunk (chunked prefill, speculative decoding);
 * :func:`gqa_append_kv` — the step before: write the new token's K/V (FP8
   quantised with per-(sequence, KV head) scales) and bump seq_lens;
 * :func:`gqa_decode_static` — gqa_decode with a fixed scratch array instead of
@@ -41,6 +43,8 @@ SIGNATURES = {
                           _I32, _I32, _I32, _VP]),
     "gqa_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
                               _I32, _I32, _I32, _I32, _I32, _I32, _VP]),
+    "gqa_decode_chunk": (_I32, [_VP, _VP, _VP, _VP, _F32, _VP, _I32, _I32,
+                                _I32, _I32, _I32, _I32, _I32, _VP]),
     "gqa_append_kv": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32,
                              _I32, _I32, _I32, _I32, _VP]),
     "gqa_decode_paged": (_I32, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _I32,
@@ -173,6 +177,32 @@ def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out=None,
                           _stream_handle(stream))
     if st != GQA_OK:
         raise GQAError(st, "gqa_decode")
+    return out
+
+
+def gqa_decode_chunk(q, k_cache, v_cache, seq_lens, scale: float, out=None,
+                     stream=None):
+    """T new tokens per sequence, causal within the chunk; q / out
+    [B, Hq, T, D], the tokens being the last T of each sequence's cache."""
+    import torch
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("seq_lens", seq_lens)):
+        _check_dev(n, t)
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, k_cache and v_cache must share a dtype")
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    B, Hq, T, D = q.shape
+    _, Hkv, Smax, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_dev("out", out)
+    st = lib().gqa_decode_chunk(q.data_ptr(), k_cache.data_ptr(),
+                                v_cache.data_ptr(), seq_lens.data_ptr(),
+                                float(scale), out.data_ptr(), B, Hq, Hkv, T,
+                                Smax, D, _dtype_code(q), _stream_handle(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_decode_chunk")
     return out
 
 
@@ -329,8 +359,12 @@ class BoundDecode:
     def __init__(self, inp: dict, out, stream=None):
         fp8 = inp.get("k_scale") is not None
         paged = inp.get("block_table") is not None
+        chunk = inp["q"].dim() == 4
         # run the full checks once, through the public entry points
-        if paged:
+        if chunk:
+            gqa_decode_chunk(inp["q"], inp["k"], inp["v"], inp["seq_lens"],
+                             inp["scale"], out=out, stream=stream)
+        elif paged:
             gqa_decode_paged(inp["q"], inp["k"], inp["v"], inp["block_table"],
                              inp["seq_lens"], inp["scale"], out=out,
                              stream=stream)
@@ -342,10 +376,16 @@ class BoundDecode:
             gqa_decode(inp["q"], inp["k"], inp["v"], inp["seq_lens"],
                        inp["scale"], out=out, stream=stream)
         q, k = inp["q"], inp["k"]
-        B, Hq, D = q.shape
+        B, Hq, D = q.shape[0], q.shape[1], q.shape[-1]
         _, Hkv, Smax, _ = k.shape
         h = _stream_handle(stream)
-        if paged:
+        if chunk:
+            self._fn = lib().gqa_decode_chunk
+            self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),
+                          inp["seq_lens"].data_ptr(), float(inp["scale"]),
+                          out.data_ptr(), B, Hq, Hkv, q.shape[2], Smax, D,
+                          _dtype_code(q), h)
+        elif paged:
             num_pages, _, page_size, _ = k.shape
             self._fn = lib().gqa_decode_paged
             self._args = (q.data_ptr(), k.data_ptr(), inp["v"].data_ptr(),
@@ -377,6 +417,9 @@ class BoundDecode:
 def decode_inputs(inp: dict, out=None, stream=None):
     """Runs the right entry point on a dict of CUDA tensors (the layout the
     input generator produces, moved to the device)."""
+    if inp["q"].dim() == 4:
+        return gqa_decode_chunk(inp["q"], inp["k"], inp["v"], inp["seq_lens"],
+                                inp["scale"], out=out, stream=stream)
     if inp.get("block_table") is not None:
         return gqa_decode_paged(inp["q"], inp["k"], inp["v"],
                                 inp["block_table"], inp["seq_lens"],

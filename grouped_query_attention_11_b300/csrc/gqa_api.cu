@@ -258,13 +258,14 @@ gqa_status launch(const void* q, const void* k, const void* v,
                   const int32_t* seq_lens, float scale, void* out, int B,
                   int Hq, int Hkv, int Smax, int D, int kv_kind, bool q_bf16,
                   void* stream_ptr, const int32_t* block_table = nullptr,
-                  int page_size = 0, int num_pages = 0) {
+                  int page_size = 0, int num_pages = 0, int T = 1) {
   const bool paged = block_table != nullptr;
   t_last_launches = 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int G = Hq / Hkv;
-  const int NHC = (G + kMaxUnitRows - 1) / kMaxUnitRows;
-  const int R = (G + NHC - 1) / NHC;
+  const int GR = G * T;  // query rows per KV head
+  const int NHC = (GR + kMaxUnitRows - 1) / kMaxUnitRows;
+  const int R = (GR + NHC - 1) / NHC;
   const int hb = R <= 16 ? 1 : (R <= 32 ? 2 : 4);
   const int rows_pad = hb * 16;
   const long long units = static_cast<long long>(B) * Hkv * NHC;
@@ -322,6 +323,8 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.Hkv = Hkv;
   p.Smax = Smax;
   p.G = G;
+  p.T = T;
+  p.GR = GR;
   p.NHC = NHC;
   p.R = R;
   p.block_table = block_table;
@@ -395,6 +398,7 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
   const int G = Hq / Hkv;
   const int NHC = (G + kMaxUnitRows - 1) / kMaxUnitRows;
   const int R = (G + NHC - 1) / NHC;
+  const int GR = G, T = 1;
   const int hb = R <= 16 ? 1 : (R <= 32 ? 2 : 4);
   const int rows_pad = hb * 16;
   const long long units = static_cast<long long>(B) * Hkv * NHC;
@@ -450,6 +454,8 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
   p.Hkv = Hkv;
   p.Smax = Smax;
   p.G = G;
+  p.T = T;
+  p.GR = GR;
   p.NHC = NHC;
   p.R = R;
 
@@ -606,6 +612,30 @@ gqa_status gqa_append_kv(const void* k_new, const void* v_new, void* k_cache,
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     t_last_launches = 1;
     return GQA_OK;
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
+}
+
+gqa_status gqa_decode_chunk(const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* seq_lens,
+                            float scale, void* out, int B, int Hq, int Hkv,
+                            int T, int Smax, int D, gqa_dtype dtype,
+                            void* stream) {
+  gqa::t_last_launches = 0;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (T < 1) return GQA_ERR_INVALID_ARG;
+  const gqa_status st = gqa::check_common(q, k_cache, v_cache, seq_lens, scale,
+                                          out, B, Hq, Hkv, Smax, D);
+  if (st != GQA_OK) return st;
+  if (static_cast<long long>(B) * Hq * T > INT32_MAX ||
+      static_cast<long long>(Hq / Hkv) * T > INT32_MAX / 2)
+    return GQA_ERR_UNSUPPORTED;
+  try {
+    return gqa::launch(q, k_cache, v_cache, nullptr, nullptr, seq_lens, scale,
+                       out, B, Hq, Hkv, Smax, D,
+                       dtype == GQA_BF16 ? gqa::kKvBF16 : gqa::kKvF16,
+                       dtype == GQA_BF16, stream, nullptr, 0, 0, T);
   } catch (...) {
     return GQA_ERR_CUDA;
   }

@@ -19,8 +19,9 @@
 //   the new row's codes are x_d / scale.
 // A sequence whose cache is full is left unchanged and raises an error bit.
 //
-// One block per sequence; the block reads L_b once, writes every head, then
-// bumps seq_lens[b], so the heads of a sequence never race on its length.
+// One block per sequence; the block reads L_b once, writes every head (16-bit
+// pieces all at once; one warp per 8-bit row), then bumps seq_lens[b], so the
+// heads of a sequence never race on its length.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -78,8 +79,6 @@ __global__ void __launch_bounds__(kAppendThreads)
     gqa_append_kernel(const AppendParams p) {
   using QT = typename std::conditional<IN_BF16, __nv_bfloat16, __half>::type;
   constexpr int kWarps = kAppendThreads / 32;
-  __shared__ float s_red[kWarps];
-  __shared__ float s_sc[2];  // the (sequence, KV head)'s old and new scale
 
   const int b = blockIdx.x, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -90,66 +89,76 @@ __global__ void __launch_bounds__(kAppendThreads)
     return;
   }
   const int D = p.D;
-  for (int j = 0; j < p.Hkv; ++j) {
-    for (int which = 0; which < 2; ++which) {
-      const size_t row = static_cast<size_t>(b) * p.Hkv + j;
-      const void* src = which ? p.v_new : p.k_new;
-      void* cache = which ? p.v_cache : p.k_cache;
-      if constexpr (!is_fp8(KV)) {
-        // 16-bit cache: copy the row, 16 bytes per thread
-        const uint4* s4 =
-            reinterpret_cast<const uint4*>(static_cast<const QT*>(src) + row * D);
-        uint4* d4 = reinterpret_cast<uint4*>(
-            static_cast<QT*>(cache) + (row * p.Smax + L) * D);
-        for (int i = tid; i < D / 8; i += kAppendThreads) d4[i] = s4[i];
+  if constexpr (!is_fp8(KV)) {
+    // 16-bit cache: every 16-byte piece of every row is independent
+    const int per_row = D / 8;
+    const int n = p.Hkv * 2 * per_row;
+    for (int i = tid; i < n; i += kAppendThreads) {
+      const int which = i / (p.Hkv * per_row);
+      const int rem = i % (p.Hkv * per_row);
+      const size_t row = static_cast<size_t>(b) * p.Hkv + rem / per_row;
+      const int c = rem % per_row;
+      const QT* src = static_cast<const QT*>(which ? p.v_new : p.k_new);
+      QT* dst = static_cast<QT*>(which ? p.v_cache : p.k_cache);
+      reinterpret_cast<uint4*>(dst + (row * p.Smax + L) * D)[c] =
+          reinterpret_cast<const uint4*>(src + row * D)[c];
+    }
+  } else {
+    // 8-bit cache: one warp per (KV head, tensor) row; lane l holds the
+    // D/32 consecutive elements l*D/32 ..
+    const float M = fp8_max_value<KV>();
+    constexpr int kMaxPer = 4;  // D / 32 for D = 128
+    const int per = D / 32;
+    for (int rw = warp; rw < p.Hkv * 2; rw += kWarps) {
+      const int which = rw / p.Hkv;
+      const size_t row = static_cast<size_t>(b) * p.Hkv + rw % p.Hkv;
+      const QT* src = static_cast<const QT*>(which ? p.v_new : p.k_new);
+      uint8_t* codes = static_cast<uint8_t*>(which ? p.v_cache : p.k_cache);
+      float* scales = which ? p.v_scale : p.k_scale;
+      float x[kMaxPer];
+      float a = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxPer; ++i) {
+        x[i] = i < per ? to_f32<QT>(src[row * D + lane * per + i]) : 0.f;
+        a = fmaxf(a, fabsf(x[i]));
+      }
+      for (int o = 16; o > 0; o >>= 1)
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      float s = 0.f, s2 = 0.f;
+      if (lane == 0) {
+        s = scales[row];
+        if (!(s > 0.f)) {
+          s2 = a > 0.f ? __fdiv_rn(a, M) : 1.f;
+        } else {
+          s2 = s;
+          for (int it = 0; it < 256 && __fdiv_rn(a, s2) > M; ++it)
+            s2 = s2 * 2.f;
+        }
+        scales[row] = s2;
+      }
+      s = __shfl_sync(0xffffffffu, s, 0);
+      s2 = __shfl_sync(0xffffffffu, s2, 0);
+      if (s > 0.f && s2 != s) {
+        // the scale grew: re-encode the L earlier tokens, 4 codes a lane
+        const float ratio = __fdiv_rn(s, s2);
+        uint32_t* w4 = reinterpret_cast<uint32_t*>(codes + row * p.Smax * D);
+        const int n4 = L * D / 4;
+        for (int i = lane; i < n4; i += 32) {
+          const uint32_t c = w4[i];
+          const float2 lo = f16x2_to_float2(fp8_lo<KV>(c));
+          const float2 hi = f16x2_to_float2(fp8_hi<KV>(c));
+          w4[i] = encode2<KV>(lo.x * ratio, lo.y * ratio) |
+                  (encode2<KV>(hi.x * ratio, hi.y * ratio) << 16);
+        }
+      }
+      uint8_t* dst = codes + (row * p.Smax + L) * D + lane * per;
+      if (per == 4) {
+        *reinterpret_cast<uint32_t*>(dst) =
+            encode2<KV>(__fdiv_rn(x[0], s2), __fdiv_rn(x[1], s2)) |
+            (encode2<KV>(__fdiv_rn(x[2], s2), __fdiv_rn(x[3], s2)) << 16);
       } else {
-        float* scales = which ? p.v_scale : p.k_scale;
-        uint8_t* codes = static_cast<uint8_t*>(cache);
-        const float M = fp8_max_value<KV>();
-        // the new row (one element per thread) and its largest magnitude
-        const float x = tid < D
-            ? to_f32<QT>(static_cast<const QT*>(src)[row * D + tid]) : 0.f;
-        float a = fabsf(x);
-        for (int o = 16; o > 0; o >>= 1)
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (lane == 0) s_red[warp] = a;
-        __syncthreads();
-        if (tid == 0) {
-          float am = s_red[0];
-          for (int w = 1; w < kWarps; ++w) am = fmaxf(am, s_red[w]);
-          const float s = scales[row];
-          float s2;
-          if (!(s > 0.f)) {
-            s2 = am > 0.f ? __fdiv_rn(am, M) : 1.f;
-          } else {
-            s2 = s;
-            for (int it = 0; it < 256 && __fdiv_rn(am, s2) > M; ++it)
-              s2 = s2 * 2.f;
-          }
-          s_sc[0] = s;
-          s_sc[1] = s2;
-        }
-        __syncthreads();
-        const float s = s_sc[0], s2 = s_sc[1];
-        if (s > 0.f && s2 != s) {
-          // the scale grew: re-encode the L earlier tokens, 4 codes a thread
-          const float ratio = __fdiv_rn(s, s2);
-          uint32_t* w4 =
-              reinterpret_cast<uint32_t*>(codes + row * p.Smax * D);
-          const int n4 = L * D / 4;
-          for (int i = tid; i < n4; i += kAppendThreads) {
-            const uint32_t c = w4[i];
-            const float2 lo = f16x2_to_float2(fp8_lo<KV>(c));
-            const float2 hi = f16x2_to_float2(fp8_hi<KV>(c));
-            w4[i] = encode2<KV>(lo.x * ratio, lo.y * ratio) |
-                    (encode2<KV>(hi.x * ratio, hi.y * ratio) << 16);
-          }
-        }
-        if (tid < D)
-          codes[(row * p.Smax + L) * D + tid] =
-              static_cast<uint8_t>(encode2<KV>(__fdiv_rn(x, s2), 0.f));
-        if (tid == 0) scales[row] = s2;
-        __syncthreads();  // s_red / s_sc are reused by the next row
+        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(
+            encode2<KV>(__fdiv_rn(x[0], s2), __fdiv_rn(x[1], s2)));
       }
     }
   }

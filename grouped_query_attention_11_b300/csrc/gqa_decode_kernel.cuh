@@ -122,8 +122,12 @@ struct DecodeParams {
   int max_pages, page_size, num_pages;
   float scale_log2;         // softmax scale * log2(e)
   int B, Hq, Hkv, Smax, G;
-  int NHC;                  // head chunks per KV head
-  int R;                    // query heads per head chunk (<= 64)
+  // Query rows: T new tokens per sequence (1 for the decode step), so every
+  // KV head serves GR = G * T rows, ordered (head in group, token); q and out
+  // are [B, Hq, T, D], in which a KV head's rows are contiguous.
+  int T, GR;
+  int NHC;                  // row chunks per KV head
+  int R;                    // query rows per chunk (<= 64)
 };
 
 // ------------------------------------------------------------ compile-time
@@ -448,7 +452,10 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
   //    so the row's weights are loaded once.  When no head block has more
   //    than 8 rows, slots e = 2, 3 (rows 8..15) are never visited.
   const int slot = whole ? 0 : cta + u;
-  const int hq0 = (j / p.NHC) * p.G + hc * p.R;  // first query head of unit
+  // the unit's first query row in q / out, in rows of D elements
+  const size_t rbase =
+      (static_cast<size_t>(bq) * p.Hq + static_cast<size_t>(j / p.NHC) * p.G) *
+          p.T + static_cast<size_t>(hc) * p.R;
   auto merge_slots = [&](auto e_count) {
     constexpr int kEs = decltype(e_count)::value;  // elements e in use
     constexpr int kSlotCount = HB * kEs * 32;
@@ -459,7 +466,7 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
       const int hbk = sl / (kEs * 32), e = (sl / 32) % kEs, ln = sl & 31;
       const int rr = (ln >> 2) + 8 * (e >> 1);
       const int row = hbk * 16 + rr;
-      if (row >= p.R || hc * p.R + row >= p.G) continue;
+      if (row >= p.R || hc * p.R + row >= p.GR) continue;
       if (row != wrow) {
         wrow = row;
 #pragma unroll
@@ -472,9 +479,7 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
         acc += wt[k] * dmp_o[warp_of(hbk, k) * 16 * D + pos];
       const int d = frag_col<kFp8, D>(n, e, ln);
       if (whole) {
-        store_out<QBF16>(
-            p.out, (static_cast<size_t>(bq) * p.Hq + hq0 + row) * D + d,
-            acc * o_mult);
+        store_out<QBF16>(p.out, (rbase + row) * D + d, acc * o_mult);
       } else {
         p.part_o[(static_cast<size_t>(slot) * C::kRowsPad + row) * D + d] =
             acc;
@@ -505,9 +510,10 @@ __device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
   const int kvh = j / p.NHC, hc = j % p.NHC;
   const float om = kFp8 ? __ldg(p.v_scale + b * p.Hkv + kvh) : 1.f;
   // valid rows of this head chunk, row-major elements (row, d)
-  const int nv = min(p.R, p.G - hc * p.R) * D;
+  const int nv = min(p.R, p.GR - hc * p.R) * D;
   const size_t h_base =
-      (static_cast<size_t>(b) * p.Hq + kvh * p.G + hc * p.R) * D;
+      ((static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.G) * p.T +
+       static_cast<size_t>(hc) * p.R) * D;
   for (int v0 = t; v0 < nv; v0 += kE * kNT) {
     float M[kE], lt[kE], acc[kE];
 #pragma unroll
@@ -766,8 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Sequences with no valid token: all-zero output rows.
     for (int b = cta; b < p.B; b += gridDim.x) {
       if (clamp_len(__ldg(p.seq_lens + b), p.Smax) != 0) continue;
-      const size_t base = static_cast<size_t>(b) * p.Hq * D;
-      for (int i = mt; i < p.Hq * D; i += kMergeThreads)
+      const size_t base = static_cast<size_t>(b) * p.Hq * p.T * D;
+      for (int i = mt; i < p.Hq * p.T * D; i += kMergeThreads)
         store_out<QBF16>(p.out, base + i, 0.f);
     }
     if (t0 >= t1) return;
@@ -823,18 +829,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   float s_mult = 0.f, o_mult = 1.f;
   bool fresh = true;
   bool aborted = false;  // this warp gave up on a wait: skip further waits
+  // Last key each of this thread's two rows may see: new token i of a chunk
+  // attends causally to keys t <= L - T + i (T = 1: every key t < L).
+  int lim0 = 0, lim1 = 0;
 
   // This thread's two fragment rows within its head block, and their query
   // rows for unit (kvh, hc) of sequence b.
   const int row0 = hb * 16 + r, row1 = row0 + 8;
   auto issue_q = [&](int b, int kvh, int hc) {
-    const bool ok0 = row0 < p.R && hc * p.R + row0 < p.G;
-    const bool ok1 = row1 < p.R && hc * p.R + row1 < p.G;
-    const int h0 = kvh * p.G + hc * p.R + row0;
-    const QT* q0 = reinterpret_cast<const QT*>(p.q) +
-                   (static_cast<size_t>(b) * p.Hq + (ok0 ? h0 : 0)) * D;
-    const QT* q1 = reinterpret_cast<const QT*>(p.q) +
-                   (static_cast<size_t>(b) * p.Hq + (ok1 ? h0 + 8 : 0)) * D;
+    const bool ok0 = row0 < p.R && hc * p.R + row0 < p.GR;
+    const bool ok1 = row1 < p.R && hc * p.R + row1 < p.GR;
+    const size_t r0 =
+        (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.G) *
+            p.T + static_cast<size_t>(hc) * p.R + row0;
+    const QT* q0 = reinterpret_cast<const QT*>(p.q) + (ok0 ? r0 : 0) * D;
+    const QT* q1 = reinterpret_cast<const QT*>(p.q) + (ok1 ? r0 + 8 : 0) * D;
     load_q_raw<kFp8, D, QT>(qf, q0, q1, ok0, ok1, cq);
   };
   issue_q(w.b, w.j / p.NHC, w.j % p.NHC);
@@ -862,6 +871,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
       m[0] = m[1] = -INFINITY;
       l[0] = l[1] = 0.f;
+      const int hc = w.j % p.NHC;
+      lim0 = w.L - p.T + (hc * p.R + row0) % p.T;
+      lim1 = w.L - p.T + (hc * p.R + row1) % p.T;
     }
 
     if (par == grp) {
@@ -876,7 +888,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = w.L;
     const int tok0 = w.ti * kTileTokens + wsl * C::kWarpTokens;  // in-seq
     const int trow0 = wsl * C::kWarpTokens;                      // in-tile
-    const bool tail = (w.ti == w.nt - 1);
+    // tiles that may hold keys a row must not see: the last one (tokens
+    // beyond L) and, for a multi-token chunk, those reaching past L - T
+    const bool tail = (w.ti == w.nt - 1) ||
+                      (w.ti * kTileTokens + kTileTokens - 1 > L - p.T);
 
     // ---- S = Q K^T for this warp's tokens ----
     float s[C::kSTiles][4];
@@ -950,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v = s[n][e] * s_mult;
         if (tail) {
           const int tk = tok0 + n * 8 + 2 * cq + (e & 1);
-          if (tk >= L) v = -INFINITY;
+          if (tk > ((e & 2) ? lim1 : lim0)) v = -INFINITY;
         }
         s[n][e] = v;
       }

@@ -119,6 +119,11 @@ WORKLOADS = {
     "llama70b_paged64_b8_s8192_bf16":
         Workload("llama70b_paged64_b8_s8192_bf16", 8, 64, 8, 128, 8192,
                  "bf16", seed=1003, page_size=64),
+    # the 70B-shaped step with 4 new tokens per sequence, causal within the
+    # chunk (speculative decoding with 4 draft tokens)
+    "llama70b_chunk4_b8_s8192_bf16":
+        Workload("llama70b_chunk4_b8_s8192_bf16", 8, 64, 8, 128, 8192,
+                 "bf16", seed=1003, T=4),
     # the same ragged batch with the other 8-bit cache format the pages name
     "ragged_e5m2_b64_h32_kv8_l500_30000":
         Workload("ragged_e5m2_b64_h32_kv8_l500_30000", 64, 32, 8, 128, 30000,

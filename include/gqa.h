@@ -121,6 +121,25 @@ gqa_status gqa_decode_fp8(const void* q, const void* k_cache,
                           gqa_dtype qo_dtype, void* stream);
 
 /*
+ * gqa_decode_chunk — T new tokens per sequence at once (chunked prefill,
+ * speculative decoding): the T tokens are the last T of the L_b =
+ * seq_lens[b] cached tokens (appended before the call), and new token i
+ * (0-based) attends causally to cached tokens t <= L_b - T + i (scaled
+ * dot-product attention with is_causal=True and GQA, "Grouped Query
+ * Attention: Why 8 KV Heads Decide Your Batch Size", The repeat_kv trap).
+ * T = 1 is gqa_decode.  A token that can see no cached token (L_b - T + i <
+ * 0) gets an all-zero output row.
+ *
+ *   q, out  [B, Hq, T, D] dtype, device, 16-byte aligned
+ *   T >= 1; other arguments as for gqa_decode (16-bit caches)
+ */
+gqa_status gqa_decode_chunk(const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* seq_lens,
+                            float scale, void* out, int B, int Hq, int Hkv,
+                            int T, int Smax, int D, gqa_dtype dtype,
+                            void* stream);
+
+/*
  * gqa_append_kv — the step before the decode: writes the new token's K and V
  * rows of every KV head into the cache at position L_b = seq_lens[b] and sets
  * seq_lens[b] = L_b + 1 ("Grouped Query Attention (GQA): Efficient Multi-Head

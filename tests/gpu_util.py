@@ -36,6 +36,11 @@ def run_cuda(inp_host: dict, out=None) -> torch.Tensor:
 
 
 def oracle_full(oracle_mod, inp: dict) -> np.ndarray:
+    if inp["q"].dim() == 4:
+        return oracle_mod.gqa_decode_chunk(inp["q"], inp["k"], inp["v"],
+                                           inp["seq_lens"], inp["scale"],
+                                           k_scale=inp["k_scale"],
+                                           v_scale=inp["v_scale"])
     if inp.get("block_table") is not None:
         return oracle_mod.gqa_decode_paged(inp["q"], inp["k"], inp["v"],
                                            inp["block_table"], inp["seq_lens"],

@@ -162,3 +162,16 @@ def test_append_rejects_invalid_arguments(L, kw):
 
 def test_append_unsupported_head_dim(L):
     assert _calla(D=96) == gq.GQA_ERR_UNSUPPORTED
+
+
+def test_decode_chunk_rejects_invalid_arguments(L):
+    lib = gq.lib()
+    assert lib.gqa_decode_chunk(A, A * 2, A * 3, A * 4, 0.125, A * 5, 2, 8, 2,
+                                0, 64, 64, gq.GQA_BF16, None) == \
+        gq.GQA_ERR_INVALID_ARG
+    assert lib.gqa_decode_chunk(A, A * 2, A * 3, A * 4, 0.125, A * 5, 2, 8, 3,
+                                2, 64, 64, gq.GQA_BF16, None) == \
+        gq.GQA_ERR_INVALID_ARG
+    assert lib.gqa_decode_chunk(A, A * 2, A * 3, A * 4, 0.125, A * 5, 2, 8, 2,
+                                2, 64, 96, gq.GQA_BF16, None) == \
+        gq.GQA_ERR_UNSUPPORTED

@@ -41,6 +41,14 @@ def test_full_size_sampled_rows(oracle_mod, name):
     out = gq.decode_inputs(dev)
     assert gq.gqa_device_errors() == 0
     assert torch.isfinite(out).all()
+    if w.T > 1:
+        # multi-token chunk: the oracle on the first and last sequences
+        sel = torch.tensor([0, w.B - 1])
+        ref = oracle_mod.gqa_decode_chunk(inp["q"][sel], inp["k"][sel],
+                                          inp["v"][sel], inp["seq_lens"][sel],
+                                          inp["scale"])
+        assert_contract(out[sel.cuda()].cpu(), ref, name)
+        return
     pairs = sample_rows(w, inp["seq_lens"], seed=w.seed)
     k = inp.get("k_contig", inp["k"])   # a paged cache, gathered
     v = inp.get("v_contig", inp["v"])

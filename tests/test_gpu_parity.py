@@ -343,3 +343,36 @@ def test_paged_bad_block_table_entry_is_flagged():
     gq.decode_inputs(dev)
     assert gq.gqa_device_errors() & 2
     assert gq.gqa_device_errors() == 0     # the query cleared it
+
+
+CHUNKS = [
+    # name, B, Hq, Hkv, D, Smax, dtype, T, lens
+    ("chunk4_bf16_g8", 3, 64, 8, 128, 700, "bf16", 4, ("list", 700, 4, 333)),
+    ("chunk16_f16_g4", 2, 16, 4, 64, 300, "f16", 16, ("list", 300, 70)),
+    ("chunk8_bf16_mqa", 2, 16, 1, 128, 200, "bf16", 8, ("list", 200, 130)),
+    ("chunk64_bf16_g2", 1, 4, 2, 64, 150, "bf16", 64, ("uniform",)),
+    ("chunk3_bf16_short", 3, 8, 2, 128, 64, "bf16", 3, ("list", 2, 0, 64)),
+    ("chunk1_is_decode", 2, 32, 8, 128, 257, "bf16", 1, ("list", 257, 9)),
+]
+
+
+@pytest.mark.parametrize("case", CHUNKS, ids=[c[0] for c in CHUNKS])
+def test_parity_chunk(oracle_mod, case):
+    name, B, Hq, Hkv, D, Smax, dt, T, lens = case
+    w = Workload(name, B, Hq, Hkv, D, Smax, dt, lens=lens,
+                 seed=4000 + CHUNKS.index(case), T=T)
+    inp = make_inputs(w, pad="nan")
+    if T == 1:
+        inp["q"] = inp["q"][:, :, None, :].contiguous()
+    dev = to_device(inp)
+    out = gq.gqa_decode_chunk(dev["q"], dev["k"], dev["v"], dev["seq_lens"],
+                              dev["scale"])
+    assert gq.gqa_last_launch_count() == 1
+    assert gq.gqa_device_errors() == 0
+    ref = oracle_mod.gqa_decode_chunk(inp["q"], inp["k"], inp["v"],
+                                      inp["seq_lens"], inp["scale"])
+    assert_close(out, ref, name)
+    if T == 1:   # the same bits as the decode step
+        d = gq.gqa_decode(dev["q"][:, :, 0].contiguous(), dev["k"], dev["v"],
+                          dev["seq_lens"], dev["scale"])
+        assert torch.equal(d.view(torch.int16), out[:, :, 0].view(torch.int16))
