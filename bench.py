@@ -48,6 +48,7 @@ L2_BYTES = 126 * 1024 * 1024
 
 
 KERNEL_SOURCES = ("gqa_decode_kernel.cuh", "ptx.cuh", "gqa_api.cu")
+GRAPH_STEPS = 100  # steps per captured CUDA graph (--graph, --op append)
 
 
 def kernel_sources_sha256() -> str:
@@ -217,7 +218,10 @@ def bench_append(a, w, name, peak, peak_kind):
     else:
         ks = vs = None
     lens = torch.full((w.B,), start_len, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
+    # a side stream: the library's per-stream scratch is set up on it before
+    # the steps are captured into graphs
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
 
     # checked once through the public wrapper, then one C-ABI call per step
     gq.gqa_append_kv(kn, vn, kc, vc, lens, k_scale=ks, v_scale=vs,
@@ -236,19 +240,33 @@ def bench_append(a, w, name, peak, peak_kind):
         if fn(*args) != gq.GQA_OK:
             raise RuntimeError("gqa_append_kv failed")
 
-    for _ in range(warmup):
-        step()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    # K steps as CUDA graphs of GRAPH_STEPS captured calls: each call is one
+    # kernel of a few microseconds, so launching them one by one from the
+    # host would time the driver's launch path, not the GPU
+    graphs, left = [], K
+    while left > 0:
+        n = min(GRAPH_STEPS, left)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                step()
+        graphs.append(g)
+        left -= n
+    lens.fill_(start_len + warmup)
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device())
-    time.sleep(0.3 if sampler.proc else 0)
+    time.sleep(1.0 if sampler.proc else 0)
     torch.cuda.synchronize()
     ev0.record(stream)
-    launches = 0
-    for _ in range(K):
-        step()
-        launches += gq.gqa_last_launch_count()
+    for g in graphs:
+        g.replay()
+    launches = K
     ev1.record(stream)
     torch.cuda.synchronize()
     sampler.stop()
@@ -266,7 +284,9 @@ def bench_append(a, w, name, peak, peak_kind):
             "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype if w.kv == "same" else
             f"{w.kv} KV / {w.dtype} rows", "data": "synthetic",
-            "config": {"workload": name, "op": "append", "B": w.B,
+            "config": {"workload": name, "op": "append",
+                       "launch": f"CUDA graphs of {GRAPH_STEPS} steps",
+                       "B": w.B,
                        "Hkv": w.Hkv, "D": w.D, "Smax": w.Smax,
                        "start_len": start_len},
             "algorithmic_bytes_per_step": algo,
@@ -380,7 +400,7 @@ def main(argv=None):
     ev1 = torch.cuda.Event(enable_timing=True)
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    time.sleep(0.3 if sampler and sampler.proc else 0)
+    time.sleep(1.0 if sampler and sampler.proc else 0)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()

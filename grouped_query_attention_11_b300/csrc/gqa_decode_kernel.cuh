@@ -87,6 +87,7 @@ constexpr int kRegsBig = 224;
 static_assert(128 * kRegsSmall + 256 * kRegsBig <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int kMaxUnitRows = 64;  // query heads per unit (4 head blocks)
+constexpr int kPrefetchTiles = 2; // tiles per block warmed in L2 at launch
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
 // Dynamic shared memory per block: the sm_100-family opt-in maximum (227 KB)
@@ -563,6 +564,47 @@ __device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
   if (t == 0) p.counters[u] = 0u;
 }
 
+// Warms L2 with this block's first tiles, guessing that every sequence fills
+// its cache (exact for uniform lengths; a wrong guess only costs bandwidth).
+// Uses kernel parameters only, so it may run before the previous kernel in
+// the stream has finished.  32-bit integer arithmetic and a fast approximate
+// divide only: a 64-bit or IEEE division here compiles to a called routine
+// that costs the whole kernel registers.  The start tile only needs to be
+// close; problems with more than 2^31 tiles skip the prefetch.
+template <int KV, int D, int HB>
+__device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
+                                                     const CUtensorMap* map_v,
+                                                     int B, int Hkv, int NHC,
+                                                     int Smax, int lane) {
+  using C = Cfg<KV, D, HB>;
+  const unsigned nt = (static_cast<unsigned>(Smax) + kTileTokens - 1) /
+                      kTileTokens;
+  const unsigned long long n64 =
+      static_cast<unsigned long long>(nt) * Hkv * NHC * B;
+  if (n64 == 0ull || n64 > 0x7fffffffull) return;
+  const unsigned per_seq = nt * Hkv * NHC;
+  const unsigned ng = static_cast<unsigned>(n64);
+  const unsigned pg = ng < gridDim.x ? ng : gridDim.x;
+  if (blockIdx.x >= pg) return;
+  // approximate start tile (no IEEE division: its slow path is a call)
+  unsigned x0 = static_cast<unsigned>(
+      __fdividef(static_cast<float>(ng), static_cast<float>(pg)) * blockIdx.x);
+  // lane k prefetches tile k of the range (one warp, no divergence in the
+  // arithmetic)
+  x0 += lane;
+  if (lane < kPrefetchTiles && x0 < ng) {
+    const unsigned bq = x0 / per_seq, rem = x0 % per_seq;
+    const int plane = static_cast<int>(bq) * Hkv +
+                      static_cast<int>(rem / nt) / NHC;
+    const int tok = static_cast<int>(rem % nt) * kTileTokens;
+#pragma unroll
+    for (int bx = 0; bx < C::kBoxesPerTile; ++bx) {
+      ptx::tma_prefetch_3d(map_k, bx * C::kBoxElems, tok, plane);
+      ptx::tma_prefetch_3d(map_v, bx * C::kBoxElems, tok, plane);
+    }
+  }
+}
+
 template <int KV, bool QBF16, int D, int HB, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap map_k,
@@ -609,10 +651,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cta = blockIdx.x;
   const int HU = p.Hkv * p.NHC;  // units per sequence
 
-  if (warp == 0 && lane == 0) {
-    // descriptor fetch overlaps the scheduler prologue
-    ptx::prefetch_tensormap(&map_k);
-    ptx::prefetch_tensormap(&map_v);
+  if (warp == 0) {
+    if (lane == 0) {
+      // descriptor fetch overlaps the scheduler prologue
+      ptx::prefetch_tensormap(&map_k);
+      ptx::prefetch_tensormap(&map_v);
+    }
+    if constexpr (!PAGED)
+      prefetch_first_tiles<KV, D, HB>(&map_k, &map_v, p.B, p.Hkv, p.NHC,
+                                      p.Smax, lane);
   }
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -830,7 +877,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool fresh = true;
   bool aborted = false;  // this warp gave up on a wait: skip further waits
   // Last key each of this thread's two rows may see: new token i of a chunk
-  // attends causally to keys t <= L - T + i (T = 1: every key t < L).
+  // attends causally to keys t <= L - T + i (T = 1: every key t < L).  The
+  // 8-bit cache kernels serve one token per sequence only (T = 1 at compile
+  // time), which keeps their register budget.
+  const int T = kFp8 ? 1 : p.T;
   int lim0 = 0, lim1 = 0;
 
   // This thread's two fragment rows within its head block, and their query
@@ -841,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok1 = row1 < p.R && hc * p.R + row1 < p.GR;
     const size_t r0 =
         (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.G) *
-            p.T + static_cast<size_t>(hc) * p.R + row0;
+            T + static_cast<size_t>(hc) * p.R + row0;
     const QT* q0 = reinterpret_cast<const QT*>(p.q) + (ok0 ? r0 : 0) * D;
     const QT* q1 = reinterpret_cast<const QT*>(p.q) + (ok1 ? r0 + 8 : 0) * D;
     load_q_raw<kFp8, D, QT>(qf, q0, q1, ok0, ok1, cq);
@@ -872,8 +922,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       m[0] = m[1] = -INFINITY;
       l[0] = l[1] = 0.f;
       const int hc = w.j % p.NHC;
-      lim0 = w.L - p.T + (hc * p.R + row0) % p.T;
-      lim1 = w.L - p.T + (hc * p.R + row1) % p.T;
+      lim0 = w.L - T + (hc * p.R + row0) % T;
+      lim1 = kFp8 ? lim0 : w.L - T + (hc * p.R + row1) % T;
     }
 
     if (par == grp) {
@@ -891,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tiles that may hold keys a row must not see: the last one (tokens
     // beyond L) and, for a multi-token chunk, those reaching past L - T
     const bool tail = (w.ti == w.nt - 1) ||
-                      (w.ti * kTileTokens + kTileTokens - 1 > L - p.T);
+                      (w.ti * kTileTokens + kTileTokens - 1 > L - T);
 
     // ---- S = Q K^T for this warp's tokens ----
     float s[C::kSTiles][4];
@@ -957,52 +1007,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- online softmax (log2 domain) ----
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    // kHi: rows r + 8 of this warp's head block are real.  When a head block
+    // has at most 8 rows they are padding: their probabilities are set to 0
+    // and their max / exp / sum work is skipped (warp-uniform choice).
+    auto softmax = [&](auto hi_c) {
+      constexpr bool kHi = decltype(hi_c)::value;
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int n = 0; n < C::kSTiles; ++n) {
+      for (int n = 0; n < C::kSTiles; ++n) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = s[n][e] * s_mult;
-        if (tail) {
-          const int tk = tok0 + n * 8 + 2 * cq + (e & 1);
-          if (tk > ((e & 2) ? lim1 : lim0)) v = -INFINITY;
+        for (int e = 0; e < (kHi ? 4 : 2); ++e) {
+          float v = s[n][e] * s_mult;
+          if (tail) {
+            const int tk = tok0 + n * 8 + 2 * cq + (e & 1);
+            if (tk > ((e & 2) ? lim1 : lim0)) v = -INFINITY;
+          }
+          s[n][e] = v;
         }
-        s[n][e] = v;
+        mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+        if (kHi) mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
       }
-      mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-    const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-    const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-    const float al0 = ptx::ex2(m[0] - base0), al1 = ptx::ex2(m[1] - base1);
-    m[0] = mn0;
-    m[1] = mn1;
-    float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-    for (int n = 0; n < C::kSTiles; ++n) {
-      s[n][0] = ptx::ex2(s[n][0] - base0);
-      s[n][1] = ptx::ex2(s[n][1] - base0);
-      s[n][2] = ptx::ex2(s[n][2] - base1);
-      s[n][3] = ptx::ex2(s[n][3] - base1);
-      rs0 += s[n][0] + s[n][1];
-      rs1 += s[n][2] + s[n][3];
-    }
-    l[0] = l[0] * al0 + rs0;
-    l[1] = l[1] * al1 + rs1;
-    if (al0 != 1.f || al1 != 1.f) {
-#pragma unroll
-      for (int n = 0; n < C::kOTiles; ++n) {
-        o[n][0] *= al0;
-        o[n][1] *= al0;
-        o[n][2] *= al1;
-        o[n][3] *= al1;
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      if (kHi) {
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       }
-    }
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float al0 = ptx::ex2(m[0] - base0);
+      const float al1 = kHi ? ptx::ex2(m[1] - base1) : 1.f;
+      m[0] = mn0;
+      m[1] = mn1;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int n = 0; n < C::kSTiles; ++n) {
+        s[n][0] = ptx::ex2(s[n][0] - base0);
+        s[n][1] = ptx::ex2(s[n][1] - base0);
+        if (kHi) {
+          s[n][2] = ptx::ex2(s[n][2] - base1);
+          s[n][3] = ptx::ex2(s[n][3] - base1);
+          rs1 += s[n][2] + s[n][3];
+        } else {
+          s[n][2] = s[n][3] = 0.f;
+        }
+        rs0 += s[n][0] + s[n][1];
+      }
+      l[0] = l[0] * al0 + rs0;
+      if (kHi) l[1] = l[1] * al1 + rs1;
+      if (al0 != 1.f || al1 != 1.f) {
+#pragma unroll
+        for (int n = 0; n < C::kOTiles; ++n) {
+          o[n][0] *= al0;
+          o[n][1] *= al0;
+          if (kHi) {
+            o[n][2] *= al1;
+            o[n][3] *= al1;
+          }
+        }
+      }
+    };
+    if (hb * 16 + 8 < p.R)
+      softmax(std::integral_constant<bool, true>{});
+    else
+      softmax(std::integral_constant<bool, false>{});
 
     // ---- O += P V ----
     constexpr bool kPBF16 = kMmaBF16;
