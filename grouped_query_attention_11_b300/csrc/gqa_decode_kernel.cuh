@@ -245,6 +245,27 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
   }
 }
 
+// Eight consecutive output elements from v * mult, one 16-byte store (idx is
+// a multiple of 8 and out 16-byte aligned).
+template <bool kBF16>
+__device__ __forceinline__ void store_out8(void* out, size_t idx,
+                                           const float (&v)[8], float mult) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (kBF16) {
+      const __nv_bfloat162 h =
+          __floats2bfloat162_rn(v[2 * i] * mult, v[2 * i + 1] * mult);
+      memcpy(&w[i], &h, 4);
+    } else {
+      const __half2 h = __floats2half2_rn(v[2 * i] * mult, v[2 * i + 1] * mult);
+      memcpy(&w[i], &h, 4);
+    }
+  }
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + idx) =
+      make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Block-wide int64 sum over all kThreads threads (uses `red` scratch).
 __device__ __forceinline__ long long block_sum(long long v, long long* red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -389,15 +410,54 @@ __device__ __forceinline__ uint32_t fp8_hi(uint32_t w) {
   }
 }
 
-// Output column d of fragment element e of O n-tile n held by lane (cq = lane
-// & 3).  The FP8 path permutes columns so that its V bytes are contiguous.
+// An item is eight consecutive output columns of one row of a head block
+// (2*D items per head block).  item_of() gives its row (0..15), its first
+// column and where its values sit in a warp's dump (fragment order, position
+// (n*4 + e)*32 + lane); dump_item() reads them.  Items are numbered so that
+// consecutive threads read distinct shared-memory banks:
+//  * 16-bit path: columns 8n .. 8n+7 of row 8*eh + q are elements e = 2eh,
+//    2eh+1 of n-tile n in lanes 4q .. 4q+3 (two float4), q fastest;
+//  * FP8 path (columns permuted): columns (2cq + ec)*D/8 + 8ng + i, i < 8,
+//    are element e = 2eh + ec of n-tiles 8ng + i in lane ln = 4*(row&7) + cq
+//    (eight scalars), lane fastest.
 template <bool kFp8, int D>
-__device__ __forceinline__ int frag_col(int n, int e, int lane) {
-  const int cq = lane & 3;
+struct FragItem {
+  int rr;    // row in the head block
+  int col0;  // first output column
+  int pos;   // dump position of the first value
+};
+
+template <bool kFp8, int D>
+__device__ __forceinline__ FragItem<kFp8, D> item_of(int i) {
+  FragItem<kFp8, D> f;
   if constexpr (!kFp8) {
-    return 8 * n + 2 * cq + (e & 1);
+    const int q = i & 7, rest = i >> 3;
+    const int n = rest % (D / 8), eh = rest / (D / 8);
+    f.rr = 8 * eh + q;
+    f.col0 = 8 * n;
+    f.pos = (n * 4 + 2 * eh) * 32 + 4 * q;
   } else {
-    return (2 * cq + (e & 1)) * (D / 8) + n;
+    const int ln = i & 31, rest = i >> 5;
+    const int ng = rest % (D / 64), r2 = rest / (D / 64);
+    const int ec = r2 & 1, eh = r2 >> 1;
+    f.rr = 8 * eh + (ln >> 2);
+    f.col0 = (2 * (ln & 3) + ec) * (D / 8) + 8 * ng;
+    f.pos = (8 * ng * 4 + 2 * eh + ec) * 32 + ln;
+  }
+  return f;
+}
+
+template <bool kFp8, int D>
+__device__ __forceinline__ void dump_item(const float* dmp, int pos,
+                                          float (&v)[8]) {
+  if constexpr (!kFp8) {
+    const float4 a = *reinterpret_cast<const float4*>(dmp + pos);
+    const float4 b = *reinterpret_cast<const float4*>(dmp + pos + 32);
+    v[0] = a.x; v[1] = b.x; v[2] = a.y; v[3] = b.y;
+    v[4] = a.z; v[5] = b.z; v[6] = a.w; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = dmp[pos + i * 128];
   }
 }
 
@@ -414,7 +474,6 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
                                            int bq, int j, bool whole, int cta) {
   using C = Cfg<KV, D, HB>;
   constexpr bool kFp8 = is_fp8(KV);
-  constexpr int kPos = C::kOTiles * 4 * 32;  // fragment positions per warp
   constexpr int kW = kGroups * C::kWarpsPerBlock;  // warps per head block
   const int kvh = j / p.NHC, hc = j % p.NHC;
   const float o_mult = kFp8 ? __ldg(p.v_scale + bq * p.Hkv + kvh) : 1.f;
@@ -448,49 +507,43 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
   }
   ptx::named_bar_sync(kBar, kNT);
 
-  // 2) merge position by position.  A fragment slot (head block, element e,
-  //    lane) is one row; a thread keeps its slot while it walks the n-tiles,
-  //    so the row's weights are loaded once.  When no head block has more
-  //    than 8 rows, slots e = 2, 3 (rows 8..15) are never visited.
+  // 2) merge item by item (eight columns of one row): the head block's
+  //    warps' dump values weighted and summed, one 16-byte output store or
+  //    two float4 partial stores.  Rows past the chunk (never dumped when a
+  //    head block has at most 8 rows) are skipped.
   const int slot = whole ? 0 : cta + u;
   // the unit's first query row in q / out, in rows of D elements
   const size_t rbase =
       (static_cast<size_t>(bq) * p.Hq + static_cast<size_t>(j / p.NHC) * p.G) *
           p.T + static_cast<size_t>(hc) * p.R;
-  auto merge_slots = [&](auto e_count) {
-    constexpr int kEs = decltype(e_count)::value;  // elements e in use
-    constexpr int kSlotCount = HB * kEs * 32;
-    float wt[kW];
-    int wrow = -1;
-    for (int wi = t; wi < kSlotCount * C::kOTiles; wi += kNT) {
-      const int sl = wi % kSlotCount, n = wi / kSlotCount;
-      const int hbk = sl / (kEs * 32), e = (sl / 32) % kEs, ln = sl & 31;
-      const int rr = (ln >> 2) + 8 * (e >> 1);
-      const int row = hbk * 16 + rr;
-      if (row >= p.R || hc * p.R + row >= p.GR) continue;
-      if (row != wrow) {
-        wrow = row;
+  constexpr int kItems = 2 * D;  // per head block
+  for (int i = t; i < HB * kItems; i += kNT) {  // warp-uniform bounds
+    const int hbk = i / kItems;
+    const FragItem<kFp8, D> f = item_of<kFp8, D>(i % kItems);
+    const int row = hbk * 16 + f.rr;
+    if (row >= p.R || hc * p.R + row >= p.GR) continue;
+    float acc[8];
 #pragma unroll
-        for (int k = 0; k < kW; ++k) wt[k] = dmp_m[warp_of(hbk, k) * 16 + rr];
-      }
-      const int pos = (n * 4 + e) * 32 + ln;
-      float acc = 0.f;
+    for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < kW; ++k) {
+      const int wk = warp_of(hbk, k);
+      const float wt = dmp_m[wk * 16 + f.rr];
+      float v[8];
+      dump_item<kFp8, D>(dmp_o + wk * 16 * D, f.pos, v);
 #pragma unroll
-      for (int k = 0; k < kW; ++k)
-        acc += wt[k] * dmp_o[warp_of(hbk, k) * 16 * D + pos];
-      const int d = frag_col<kFp8, D>(n, e, ln);
-      if (whole) {
-        store_out<QBF16>(p.out, (rbase + row) * D + d, acc * o_mult);
-      } else {
-        p.part_o[(static_cast<size_t>(slot) * C::kRowsPad + row) * D + d] =
-            acc;
-      }
+      for (int x = 0; x < 8; ++x) acc[x] += wt * v[x];
     }
-  };
-  if (HB == 1 && p.R <= 8)
-    merge_slots(std::integral_constant<int, 2>{});
-  else
-    merge_slots(std::integral_constant<int, 4>{});
+    if (whole) {
+      store_out8<QBF16>(p.out, (rbase + row) * D + f.col0, acc, o_mult);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(
+          p.part_o + (static_cast<size_t>(slot) * C::kRowsPad + row) * D +
+          f.col0);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
   if (!whole)
     for (int row = t; row < HB * 16; row += kNT)
       p.part_lse[static_cast<size_t>(slot) * C::kRowsPad + row] =
@@ -499,66 +552,83 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
 }
 
 // Split combine of unit u (covered by blocks cf..cl): the output rows from
-// all partials, one pass with a running maximum, the loads of kB partials x
-// kE elements per thread in flight together.  Run by kNT threads.
-template <int KV, bool QBF16, int D, int HB, int kNT, int kE>
+// all partials, one pass with a running maximum.  A thread takes kI items of
+// eight columns (two float4 of a row) and loads them from kB partials at a
+// time, all in flight together.  Run by kNT threads.
+template <int KV, bool QBF16, int D, int HB, int kNT>
 __device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
                                              int u, int b, int j, int cf,
                                              int cl) {
   using C = Cfg<KV, D, HB>;
   constexpr bool kFp8 = is_fp8(KV);
-  constexpr int kB = 4;
+  constexpr int kB = 4;       // partials per batch
+  constexpr int kI = 2;       // items per thread per pass
+  constexpr int kG = D / 8;   // items per row
   const int kvh = j / p.NHC, hc = j % p.NHC;
   const float om = kFp8 ? __ldg(p.v_scale + b * p.Hkv + kvh) : 1.f;
-  // valid rows of this head chunk, row-major elements (row, d)
-  const int nv = min(p.R, p.GR - hc * p.R) * D;
+  const int n_items = min(p.R, p.GR - hc * p.R) * kG;  // valid rows only
   const size_t h_base =
       ((static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.G) * p.T +
        static_cast<size_t>(hc) * p.R) * D;
-  for (int v0 = t; v0 < nv; v0 += kE * kNT) {
-    float M[kE], lt[kE], acc[kE];
+  for (int i0 = t; i0 < n_items; i0 += kI * kNT) {
+    float M[kI], lt[kI], acc[kI][8];
 #pragma unroll
-    for (int x = 0; x < kE; ++x) {
+    for (int x = 0; x < kI; ++x) {
       M[x] = -INFINITY;
       lt[x] = 0.f;
-      acc[x] = 0.f;
+#pragma unroll
+      for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
     }
     for (int c0 = cf; c0 <= cl; c0 += kB) {
-      float ls[kB][kE], ov[kB][kE];
+      float ls[kB][kI];
+      float4 ov[kB][kI][2];
 #pragma unroll
       for (int k = 0; k < kB; ++k)
 #pragma unroll
-        for (int x = 0; x < kE; ++x) {
-          const int v = v0 + x * kNT;
-          const bool ok = c0 + k <= cl && v < nv;
-          const size_t sl = static_cast<size_t>(c0 + k + u);
-          ls[k][x] =
-              ok ? __ldcg(p.part_lse + sl * C::kRowsPad + v / D) : -INFINITY;
-          ov[k][x] = ok ? __ldcg(p.part_o + sl * C::kRowsPad * D + v) : 0.f;
+        for (int x = 0; x < kI; ++x) {
+          const int it = i0 + x * kNT;
+          const bool ok = c0 + k <= cl && it < n_items;
+          const size_t row =
+              static_cast<size_t>(c0 + k + u) * C::kRowsPad + it / kG;
+          const float4* src = reinterpret_cast<const float4*>(
+              p.part_o + row * D + (it % kG) * 8);
+          ls[k][x] = ok ? __ldcg(p.part_lse + row) : -INFINITY;
+          ov[k][x][0] = ok ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+          ov[k][x][1] = ok ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-      for (int x = 0; x < kE; ++x) {
-        const float Mn = fmaxf(
-            M[x], fmaxf(fmaxf(ls[0][x], ls[1][x]), fmaxf(ls[2][x], ls[3][x])));
+      for (int x = 0; x < kI; ++x) {
+        float Mn = M[x];
+#pragma unroll
+        for (int k = 0; k < kB; ++k) Mn = fmaxf(Mn, ls[k][x]);
         if (Mn == -INFINITY) continue;
         const float a = ptx::ex2(M[x] - Mn);  // 0 while M is -inf
         lt[x] *= a;
-        acc[x] *= a;
+#pragma unroll
+        for (int y = 0; y < 8; ++y) acc[x][y] *= a;
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
           const float f = ptx::ex2(ls[k][x] - Mn);
           lt[x] += f;
-          acc[x] += f * ov[k][x];
+          acc[x][0] += f * ov[k][x][0].x;
+          acc[x][1] += f * ov[k][x][0].y;
+          acc[x][2] += f * ov[k][x][0].z;
+          acc[x][3] += f * ov[k][x][0].w;
+          acc[x][4] += f * ov[k][x][1].x;
+          acc[x][5] += f * ov[k][x][1].y;
+          acc[x][6] += f * ov[k][x][1].z;
+          acc[x][7] += f * ov[k][x][1].w;
         }
         M[x] = Mn;
       }
     }
 #pragma unroll
-    for (int x = 0; x < kE; ++x) {
-      const int v = v0 + x * kNT;
-      if (v < nv)
-        store_out<QBF16>(p.out, h_base + v,
-                         (lt[x] > 0.f ? acc[x] / lt[x] : 0.f) * om);
+    for (int x = 0; x < kI; ++x) {
+      const int it = i0 + x * kNT;
+      if (it < n_items)
+        store_out8<QBF16>(p.out, h_base + static_cast<size_t>(it / kG) * D +
+                                     (it % kG) * 8,
+                          acc[x], (lt[x] > 0.f ? 1.f / lt[x] : 0.f) * om);
     }
   }
   if (t == 0) p.counters[u] = 0u;
@@ -1224,38 +1294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_q(wn.b, wn.j / p.NHC, wn.j % p.NHC);
         fresh = true;
       } else {
-        // ---- the block's last unit: all consumer threads merge it ----
-        const int ct = tid - kFirstConsumerWarp * 32;  // 0 .. 255
-        ptx::named_bar_sync(1, kConsumerThreads);  // every warp's dump
-        const bool whole = (c_first == c_last);
-        merge_unit<KV, QBF16, D, HB, kConsumerThreads, 1>(
-            ct, dmp_o, dmp_m, dmp_l, s_rowlse, p, u, w.b, w.j, whole, cta);
-        if (ct == 0) {
-          if (!whole && s_npend < 2) {
-            const int k = s_npend;
-            s_pend_t[k] = ptx::atom_add_acq_rel_gpu(p.counters + u, 1u);
-            s_pend_u[k] = u;
-            s_pend_b[k] = w.b;
-            s_pend_j[k] = w.j;
-            s_pend_cf[k] = c_first;
-            s_pend_cl[k] = c_last;
-            s_npend = k + 1;
-          }
-          // last arrival of a unit: this block combines its partials
-          // (the acquire side of both adds: what the other blocks released
-          // before their arrivals is visible to this thread, and to the
-          // others through the barrier below)
-          for (int i = 0; i < 2; ++i)
-            s_pend_last[i] =
-                i < s_npend && s_pend_t[i] == static_cast<uint32_t>(
-                                                  s_pend_cl[i] - s_pend_cf[i]);
-        }
-        ptx::named_bar_sync(1, kConsumerThreads);
-        for (int i = 0; i < 2; ++i)
-          if (s_pend_last[i])  // uniform
-            combine_unit<KV, QBF16, D, HB, kConsumerThreads, 4>(
-                ct, p, s_pend_u[i], s_pend_b[i], s_pend_j[i], s_pend_cf[i],
-                s_pend_cl[i]);
+        break;  // g == t1 - 1: the block's range is done
       }
     }
     par ^= 1;
@@ -1265,6 +1304,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     w.next(p, HU);
   }
+
+  // ---- the block's last unit: all consumer threads merge it, then run the
+  // split combines of the units whose last arrival was this block's.  After
+  // the tile loop, so that none of its registers are live; the unit's
+  // descriptor is in shared memory (written before the dump's arrival). ----
+  const int ct = tid - kFirstConsumerWarp * 32;  // 0 .. 255
+  ptx::named_bar_sync(1, kConsumerThreads);  // every warp's dump
+  {
+    const int u = s_du, c_first = s_dcf, c_last = s_dcl;
+    const bool whole = (c_first == c_last);
+    merge_unit<KV, QBF16, D, HB, kConsumerThreads, 1>(
+        ct, dmp_o, dmp_m, dmp_l, s_rowlse, p, u, s_db, s_dj, whole, cta);
+    if (ct == 0) {
+      if (!whole && s_npend < 2) {
+        const int k = s_npend;
+        s_pend_t[k] = ptx::atom_add_acq_rel_gpu(p.counters + u, 1u);
+        s_pend_u[k] = u;
+        s_pend_b[k] = s_db;
+        s_pend_j[k] = s_dj;
+        s_pend_cf[k] = c_first;
+        s_pend_cl[k] = c_last;
+        s_npend = k + 1;
+      }
+      // last arrival of a unit: this block combines its partials
+      // (the acquire side of both adds: what the other blocks released
+      // before their arrivals is visible to this thread, and to the
+      // others through the barrier below)
+      for (int i = 0; i < 2; ++i)
+        s_pend_last[i] =
+            i < s_npend && s_pend_t[i] == static_cast<uint32_t>(
+                                              s_pend_cl[i] - s_pend_cf[i]);
+    }
+    ptx::named_bar_sync(1, kConsumerThreads);
+  }
+  for (int i = 0; i < 2; ++i)
+    if (s_pend_last[i])  // uniform
+      combine_unit<KV, QBF16, D, HB, kConsumerThreads>(
+          ct, p, s_pend_u[i], s_pend_b[i], s_pend_j[i], s_pend_cf[i],
+          s_pend_cl[i]);
 }
 
 }  // namespace gqa
