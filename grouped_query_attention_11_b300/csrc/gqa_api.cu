@@ -250,6 +250,28 @@ gqa_status check_common(const void* q, const void* k, const void* v,
   return GQA_OK;
 }
 
+// Block count that lines block ranges up with unit boundaries when every
+// sequence has the same number of tiles (the kernel checks that on the
+// device): the largest P of at least 5/6 of the grid that is a multiple of
+// the unit count or divides it.  Fewer blocks stream more bytes each, so
+// this pays where the cuts it removes are a large share of a block's work:
+//  * P = units (one unit per block) or P = units / k for k <= 4;
+//  * P = k * units for k > 1 (every unit split over k blocks) only for
+//    64-row units (hb == 4), whose partials are the costliest to merge when
+//    the cuts fall anywhere.
+// 0: no such P.
+int aligned_blocks(long long units, int grid, int hb) {
+  const int min_p = grid - grid / 6;
+  if (units <= grid) {
+    const int k = grid / static_cast<int>(units);
+    const int pa = k * static_cast<int>(units);
+    return (pa >= min_p && (k == 1 || hb == 4)) ? pa : 0;
+  }
+  for (int d = grid; d >= min_p; --d)
+    if (units % d == 0) return units / d <= 4 ? d : 0;
+  return 0;
+}
+
 // Smax: the cache's token capacity per sequence.  A paged cache passes its
 // block table, page size and page count (Smax = max_pages * page_size);
 // block_table == nullptr is a contiguous cache.
@@ -327,6 +349,7 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.GR = GR;
   p.NHC = NHC;
   p.R = R;
+  p.p_align = g_num_ctas_override > 0 ? 0 : aligned_blocks(units, grid, hb);
   p.block_table = block_table;
   p.max_pages = paged ? Smax / page_size : 0;
   p.page_size = page_size;
@@ -458,6 +481,7 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
   p.GR = GR;
   p.NHC = NHC;
   p.R = R;
+  p.p_align = g_num_ctas_override > 0 ? 0 : aligned_blocks(units, grid, hb);
 
   var.fn<<<grid, kThreads, var.smem, stream>>>(map_k, map_v, p);
   if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;

@@ -129,6 +129,10 @@ struct DecodeParams {
   int T, GR;
   int NHC;                  // row chunks per KV head
   int R;                    // query rows per chunk (<= 64)
+  // Blocks to use when every sequence has the same number of tiles, chosen
+  // by the host so that block ranges line up with unit boundaries (0: none;
+  // then min(grid, tiles) blocks take part).
+  int p_align;
 };
 
 // ------------------------------------------------------------ compile-time
@@ -645,7 +649,8 @@ template <int KV, int D, int HB>
 __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
                                                      const CUtensorMap* map_v,
                                                      int B, int Hkv, int NHC,
-                                                     int Smax, int lane) {
+                                                     int Smax, int p_align,
+                                                     int lane) {
   using C = Cfg<KV, D, HB>;
   const unsigned nt = (static_cast<unsigned>(Smax) + kTileTokens - 1) /
                       kTileTokens;
@@ -654,7 +659,8 @@ __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
   if (n64 == 0ull || n64 > 0x7fffffffull) return;
   const unsigned per_seq = nt * Hkv * NHC;
   const unsigned ng = static_cast<unsigned>(n64);
-  const unsigned pg = ng < gridDim.x ? ng : gridDim.x;
+  unsigned pg = ng < gridDim.x ? ng : gridDim.x;
+  if (p_align > 0 && ng >= static_cast<unsigned>(p_align)) pg = p_align;
   if (blockIdx.x >= pg) return;
   // approximate start tile (no IEEE division: its slow path is a call)
   unsigned x0 = static_cast<unsigned>(
@@ -704,6 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_b0;
   __shared__ int s_found;
   __shared__ volatile int s_abort;
+  // the flat list's tile count and the blocks taking part, re-read at unit
+  // ends (volatile: not held in registers through the tile loop)
+  __shared__ volatile long long s_N;
+  __shared__ volatile int s_P;
   __shared__ float s_rowlse[HB * 16];   // log2-sum-exp per merged row
   // descriptor of the unit whose states are in the dump area; s_dstop marks
   // the block's last unit, which the consumers merge themselves
@@ -729,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (!PAGED)
       prefetch_first_tiles<KV, D, HB>(&map_k, &map_v, p.B, p.Hkv, p.NHC,
-                                      p.Smax, lane);
+                                      p.Smax, p.p_align, lane);
   }
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -760,12 +770,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.B <= kThreads) {
     // one load of seq_lens and one block scan give everything
     const int b = tid;
-    const long long v =
-        b < p.B ? static_cast<long long>(
-                      tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU
-                : 0;
+    const int nt_b =
+        b < p.B ? tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax)) : 0;
+    const int nt_0 = tiles_of(clamp_len(__ldg(p.seq_lens), p.Smax));
+    const long long v = static_cast<long long>(nt_b) * HU;
     const long long incl = block_incl_scan(v, s_red, &N);
+    // equal tile counts: the host's unit-aligned block count applies
+    const bool uniform = __syncthreads_and(b >= p.B || nt_b == nt_0) != 0;
     P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
+    if (uniform && p.p_align > 0 && N >= p.p_align) P = p.p_align;
     if (cta < P) {
       t0 = N * cta / P;
       t1 = N * (cta + 1) / P;
@@ -806,6 +819,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s_found) break;
       }
     }
+  }
+  if (tid == 0) {
+    s_N = N;
+    s_P = P;
   }
   __syncthreads();
 
@@ -1275,8 +1292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool last = (g == t1 - 1);
       const long long us = w.pref + static_cast<long long>(w.j) * w.nt;
       const int u = w.b * HU + w.j;
-      const int c_first = block_of_tile(us, N, P);
-      const int c_last = block_of_tile(us + w.nt - 1, N, P);
+      const long long Nv = s_N;
+      const int Pv = s_P;
+      const int c_first = block_of_tile(us, Nv, Pv);
+      const int c_last = block_of_tile(us + w.nt - 1, Nv, Pv);
       if (cw == 0 && lane == 0) {
         s_du = u;
         s_db = w.b;
