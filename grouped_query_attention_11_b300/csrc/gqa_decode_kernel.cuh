@@ -18,8 +18,8 @@
 //    number of KV bytes (+-1 tile), whatever the length mix.  A unit cut by a
 //    range boundary is finished by the fused split combine below.
 //  * Warp roles.  A block is three warpgroups.  Warpgroup 0: one producer
-//    warp and three merge warps; warpgroups 1 and 2: the two ping-pong
-//    consumer groups.  setmaxnreg moves registers from warpgroup 0 (56 per
+//    warp and three merge warps; warpgroups 1 and 2: eight consumer warps.
+//    setmaxnreg moves registers from warpgroup 0 (56 per
 //    thread) to the consumers (224), whose mma fragments, accumulators and
 //    query rows then never spill.
 //  * KV stream.  The producer warp issues TMA tensor loads (128-byte
@@ -31,11 +31,13 @@
 //    QK^T and PV through mma.sync m16n8k16 with fp32 accumulation.  The online
 //    softmax (running row max, rescale, row sum) lives in registers; row
 //    reductions are two quad shuffles.
-//  * Ping-pong consumers.  Two groups of four consumer warps take alternate
-//    ring stages, each with its own softmax state, so that one group's
-//    dependent mma / exp chains overlap the other's.
+//  * Consumer groups.  The consumer warps form groups (two of four warps, or
+//    four of two for the 8-bit caches with one head block) that take the
+//    ring's stages in turn, each with its own softmax state, so that one
+//    group's dependent mma / exp chains overlap the others'.
 //  * Asynchronous unit epilogue.  At the end of a unit every consumer warp
-//    only dumps its softmax state to shared memory (mma fragment order) and
+//    only dumps its softmax state to shared memory (its rows normalised,
+//    row-major) and
 //    signals an mbarrier; it goes straight on with the next unit, whose query
 //    rows it has already started loading.  The merge warps combine the eight
 //    states, write the output rows or a split partial, and publish the
@@ -70,9 +72,9 @@
 namespace gqa {
 
 constexpr int kTileTokens = 64;   // tokens per pipeline stage
-constexpr int kGroupWarps = 4;     // consumer warps per ping-pong group
-constexpr int kGroups = 2;         // groups taking alternate ring stages
-constexpr int kConsumerWarps = kGroups * kGroupWarps;
+// Eight consumer warps, split into groups that take the ring's tiles in turn
+// (per variant: two groups of four warps, or four of two; see Cfg).
+constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kMergeWarps = 3;     // warps 1..3 of warpgroup 0
 constexpr int kMergeThreads = kMergeWarps * 32;
@@ -91,8 +93,8 @@ constexpr int kPrefetchTiles = 2; // tiles per block warmed in L2 at launch
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
 // Dynamic shared memory per block: the sm_100-family opt-in maximum (227 KB)
-// less 1 KB left for the kernel's static shared variables.
-constexpr int kSmemBudget = 232448 - 1024;
+// less 512 bytes left for the kernel's static shared variables.
+constexpr int kSmemBudget = 232448 - 512;
 
 enum KvKind : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2, kKvE5M2 = 3 };
 
@@ -148,6 +150,12 @@ struct Cfg {
   static constexpr int kBoxElems = is_fp8(KV) ? D : 64;
   static constexpr int kBoxBytes = kTileTokens * kBoxElems * kElemBytes;
   static constexpr int kBoxesPerTile = D / kBoxElems;
+  // Consumer groups: four of two warps for the 8-bit caches with one head
+  // block, whose warps are bound by their dequantising arithmetic (32 tokens
+  // a warp per tile: more independent work per softmax round); otherwise two
+  // of four warps.
+  static constexpr int kGroups = (is_fp8(KV) && HB == 1) ? 4 : 2;
+  static constexpr int kGroupWarps = kConsumerWarps / kGroups;
   static constexpr int kWarpsPerBlock = kGroupWarps / HB;  // per head block
   static constexpr int kWarpTokens = kTileTokens / kWarpsPerBlock;
   static constexpr int kSTiles = kWarpTokens / 8;   // S n-tiles per warp
@@ -155,19 +163,27 @@ struct Cfg {
   static constexpr int kOTiles = D / 8;             // O n-tiles
   static constexpr int kQSteps = D / 16;            // QK k-steps
   static constexpr int kRowsPad = HB * 16;
+  // Unit dump: per consumer warp its 16 rows of normalised O, row-major, in
+  // f16 for the 8-bit caches (values bounded by the code range) and fp32
+  // otherwise; then the row maxima and row sums.
+  using DumpT = typename std::conditional<is_fp8(KV), __half, float>::type;
+  static constexpr int kDumpRowBytes = D * static_cast<int>(sizeof(DumpT));
+  static constexpr int kDumpWarpBytes = 16 * kDumpRowBytes;
   static constexpr int kMergeBytes =
-      kConsumerWarps * 16 * D * 4 + 2 * kConsumerWarps * 16 * 4;
+      kConsumerWarps * kDumpWarpBytes + 2 * kConsumerWarps * 16 * 4;
   static constexpr int kStagesRaw = (kSmemBudget - kMergeBytes - 1024 - 256) /
                                     kStageBytes;
-  // Even, so that stage s is always consumed by ping-pong group s % 2: each
-  // group then waits on the phases of its stages strictly in order, which the
-  // mbarrier parity test requires.
-  static constexpr int kStages = (kStagesRaw > 16 ? 16 : kStagesRaw) & ~1;
+  // A multiple of the group count, so that stage s is always consumed by
+  // group s % kGroups: each group then waits on the phases of its stages
+  // strictly in order, which the mbarrier parity test requires.
+  static constexpr int kStages =
+      (kStagesRaw > 16 ? 16 : kStagesRaw) / kGroups * kGroups;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kRingBytes +
                                     kMergeBytes + 2 * kStages * 8 + 64;
-  static_assert(kStages >= 2 && kStages % 2 == 0,
-                "pipeline needs an even number (>= 2) of stages");
+  static_assert(kStages >= 2 * kGroups && kStages % kGroups == 0,
+                "pipeline needs two stages per group");
+  static_assert(kWarpsPerBlock >= 1, "a head block needs a warp per group");
   static_assert(kSTiles % 2 == 0 && kPSteps >= 1, "warp tile shape");
   static_assert(kQSteps % 2 == 0, "QK k-steps are split into two chains");
   // Short accumulator chains: with few S tiles per warp the QK k-loop is
@@ -414,54 +430,38 @@ __device__ __forceinline__ uint32_t fp8_hi(uint32_t w) {
   }
 }
 
-// An item is eight consecutive output columns of one row of a head block
-// (2*D items per head block).  item_of() gives its row (0..15), its first
-// column and where its values sit in a warp's dump (fragment order, position
-// (n*4 + e)*32 + lane); dump_item() reads them.  Items are numbered so that
-// consecutive threads read distinct shared-memory banks:
-//  * 16-bit path: columns 8n .. 8n+7 of row 8*eh + q are elements e = 2eh,
-//    2eh+1 of n-tile n in lanes 4q .. 4q+3 (two float4), q fastest;
-//  * FP8 path (columns permuted): columns (2cq + ec)*D/8 + 8ng + i, i < 8,
-//    are element e = 2eh + ec of n-tiles 8ng + i in lane ln = 4*(row&7) + cq
-//    (eight scalars), lane fastest.
-template <bool kFp8, int D>
-struct FragItem {
-  int rr;    // row in the head block
-  int col0;  // first output column
-  int pos;   // dump position of the first value
-};
-
-template <bool kFp8, int D>
-__device__ __forceinline__ FragItem<kFp8, D> item_of(int i) {
-  FragItem<kFp8, D> f;
-  if constexpr (!kFp8) {
-    const int q = i & 7, rest = i >> 3;
-    const int n = rest % (D / 8), eh = rest / (D / 8);
-    f.rr = 8 * eh + q;
-    f.col0 = 8 * n;
-    f.pos = (n * 4 + 2 * eh) * 32 + 4 * q;
-  } else {
-    const int ln = i & 31, rest = i >> 5;
-    const int ng = rest % (D / 64), r2 = rest / (D / 64);
-    const int ec = r2 & 1, eh = r2 >> 1;
-    f.rr = 8 * eh + (ln >> 2);
-    f.col0 = (2 * (ln & 3) + ec) * (D / 8) + 8 * ng;
-    f.pos = (8 * ng * 4 + 2 * eh + ec) * 32 + ln;
-  }
-  return f;
+// Byte offset of the 16-byte chunk c of dump row `row` (row-major rows of
+// kRowBytes; chunks XOR-swizzled by row & 7 so that the eight rows a warp
+// writes or reads together fall in different banks).
+template <int kRowBytes>
+__device__ __forceinline__ int dump_off(int row, int c) {
+  return row * kRowBytes + ((c ^ (row & 7)) << 4);
 }
 
-template <bool kFp8, int D>
-__device__ __forceinline__ void dump_item(const float* dmp, int pos,
+// Eight consecutive values (columns 8n .. 8n+7) of dump row `row`.
+template <typename DumpT, int D>
+__device__ __forceinline__ void dump_load8(const uint8_t* w, int row, int n,
                                           float (&v)[8]) {
-  if constexpr (!kFp8) {
-    const float4 a = *reinterpret_cast<const float4*>(dmp + pos);
-    const float4 b = *reinterpret_cast<const float4*>(dmp + pos + 32);
-    v[0] = a.x; v[1] = b.x; v[2] = a.y; v[3] = b.y;
-    v[4] = a.z; v[5] = b.z; v[6] = a.w; v[7] = b.w;
+  constexpr int kRowBytes = D * static_cast<int>(sizeof(DumpT));
+  if constexpr (std::is_same<DumpT, float>::value) {
+    const float4 a =
+        *reinterpret_cast<const float4*>(w + dump_off<kRowBytes>(row, 2 * n));
+    const float4 b = *reinterpret_cast<const float4*>(
+        w + dump_off<kRowBytes>(row, 2 * n + 1));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   } else {
+    const uint4 a =
+        *reinterpret_cast<const uint4*>(w + dump_off<kRowBytes>(row, n));
+    const uint32_t x[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = dmp[pos + i * 128];
+    for (int i = 0; i < 4; ++i) {
+      __half2 h;
+      memcpy(&h, &x[i], 4);
+      const float2 f = __half22float2(h);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
   }
 }
 
@@ -471,24 +471,25 @@ __device__ __forceinline__ void dump_item(const float* dmp, int pos,
 // its normalised partial (row-major fp32 + log2-sum-exp per row).  Run by
 // kNT threads (t = 0 .. kNT-1) that synchronise on named barrier kBar.
 template <int KV, bool QBF16, int D, int HB, int kNT, int kBar>
-__device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
+__device__ __forceinline__ void merge_unit(int t, const uint8_t* dmp_o,
                                            float* dmp_m, const float* dmp_l,
                                            float* s_rowlse,
                                            const DecodeParams& p, int u,
                                            int bq, int j, bool whole, int cta) {
   using C = Cfg<KV, D, HB>;
   constexpr bool kFp8 = is_fp8(KV);
-  constexpr int kW = kGroups * C::kWarpsPerBlock;  // warps per head block
+  constexpr int kW = C::kGroups * C::kWarpsPerBlock;  // warps per head block
   const int kvh = j / p.NHC, hc = j % p.NHC;
   const float o_mult = kFp8 ? __ldg(p.v_scale + bq * p.Hkv + kvh) : 1.f;
   // the k-th warp of head block hbk
   auto warp_of = [](int hbk, int k) {
-    return (k / C::kWarpsPerBlock) * kGroupWarps + hbk * C::kWarpsPerBlock +
+    return (k / C::kWarpsPerBlock) * C::kGroupWarps + hbk * C::kWarpsPerBlock +
            k % C::kWarpsPerBlock;
   };
 
   // 1) per merged row: the max over the head block's warps, the total, and
-  //    each warp's weight exp2(m_w - M) / total (written over m_w).  One
+  //    each warp's weight exp2(m_w - M) * l_w / total (written over m_w; the
+  //    dumped rows are normalised by their own sums l_w).  One
   //    thread per (row, warp); the kW threads of a row are adjacent lanes and
   //    reduce with shuffles.
   static_assert(32 % kW == 0, "a row's warps must share a warp of threads");
@@ -506,7 +507,7 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
     float lt = lv * f;
 #pragma unroll
     for (int o = 1; o < kW; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
-    dmp_m[wk * 16 + rr] = lt > 0.f ? f / lt : 0.f;
+    dmp_m[wk * 16 + rr] = lt > 0.f ? f * lv / lt : 0.f;
     if (k == 0) s_rowlse[row] = lt > 0.f ? Mb + ptx::lg2(lt) : -INFINITY;
   }
   ptx::named_bar_sync(kBar, kNT);
@@ -520,11 +521,11 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
   const size_t rbase =
       (static_cast<size_t>(bq) * p.Hq + static_cast<size_t>(j / p.NHC) * p.G) *
           p.T + static_cast<size_t>(hc) * p.R;
-  constexpr int kItems = 2 * D;  // per head block
+  constexpr int kItems = 2 * D;  // per head block: 16 rows x D/8 columns
   for (int i = t; i < HB * kItems; i += kNT) {  // warp-uniform bounds
     const int hbk = i / kItems;
-    const FragItem<kFp8, D> f = item_of<kFp8, D>(i % kItems);
-    const int row = hbk * 16 + f.rr;
+    const int rr = i & 15, n = (i % kItems) >> 4;  // row fastest: no conflicts
+    const int row = hbk * 16 + rr;
     if (row >= p.R || hc * p.R + row >= p.GR) continue;
     float acc[8];
 #pragma unroll
@@ -532,18 +533,19 @@ __device__ __forceinline__ void merge_unit(int t, const float* dmp_o,
 #pragma unroll 1
     for (int k = 0; k < kW; ++k) {
       const int wk = warp_of(hbk, k);
-      const float wt = dmp_m[wk * 16 + f.rr];
+      const float wt = dmp_m[wk * 16 + rr];
       float v[8];
-      dump_item<kFp8, D>(dmp_o + wk * 16 * D, f.pos, v);
+      dump_load8<typename C::DumpT, D>(dmp_o + wk * C::kDumpWarpBytes, rr, n,
+                                       v);
 #pragma unroll
       for (int x = 0; x < 8; ++x) acc[x] += wt * v[x];
     }
     if (whole) {
-      store_out8<QBF16>(p.out, (rbase + row) * D + f.col0, acc, o_mult);
+      store_out8<QBF16>(p.out, (rbase + row) * D + 8 * n, acc, o_mult);
     } else {
       float4* dst = reinterpret_cast<float4*>(
           p.part_o + (static_cast<size_t>(slot) * C::kRowsPad + row) * D +
-          f.col0);
+          8 * n);
       dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
@@ -698,8 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem;
   // Dump area of the unit epilogue: per consumer warp its O fragments
   // (position (n*4 + e)*32 + lane), row maxima and row sums.
-  float* dmp_o = reinterpret_cast<float*>(ring + C::kRingBytes);
-  float* dmp_m = dmp_o + kConsumerWarps * 16 * D;
+  uint8_t* dmp_o = ring + C::kRingBytes;
+  float* dmp_m = reinterpret_cast<float*>(dmp_o + kConsumerWarps * C::kDumpWarpBytes);
   float* dmp_l = dmp_m + kConsumerWarps * 16;
   uint64_t* full = reinterpret_cast<uint64_t*>(dmp_l + kConsumerWarps * 16);
   uint64_t* empty = full + C::kStages;
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], kGroupWarps);
+      ptx::mbar_init(&empty[s], C::kGroupWarps);
     }
     ptx::mbar_init(dump_full, kConsumerWarps);
     ptx::mbar_init(dump_empty, 1);
@@ -949,8 +951,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // =============================== consumers ================================
   const int cw = warp - kFirstConsumerWarp;  // consumer warp 0..7
-  const int grp = cw / kGroupWarps;          // ping-pong group
-  const int lw = cw % kGroupWarps;           // warp within the group
+  const int grp = cw / C::kGroupWarps;       // consumer group
+  const int lw = cw % C::kGroupWarps;        // warp within the group
   const int hb = lw / C::kWarpsPerBlock;     // head block of this warp
   const int wsl = lw % C::kWarpsPerBlock;    // token slice of this warp
   const int r = lane >> 2, cq = lane & 3;    // mma fragment coordinates
@@ -987,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int stage = 0;     // ring stage of tile g: (g - t0) % kStages
   uint32_t ph = 0;   // its phase parity: ((g - t0) / kStages) & 1
-  int par = 0;       // (g - t0) & 1: the group that computes tile g
+  int par = 0;       // (g - t0) % kGroups: the group that computes tile g
   uint32_t dph = 0;  // parity of this block's unit epilogues so far
   for (long long g = t0; g < t1; ++g) {
     const int kvh = w.j / p.NHC;
@@ -1014,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (par == grp) {
-    // ---- wait for the stage (tiles alternate between the two groups) ----
+    // ---- wait for the stage (the groups take the tiles in turn) ----
     if (!aborted && !ptx::mbar_wait_bounded(&full[stage], ph, kWaitLimitNs)) {
       atomicOr(p.error, kErrWaitTimeout);
       aborted = true;
@@ -1273,14 +1275,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 1);
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
       const bool hi_rows = hb * 16 + 8 < p.R;  // rows r+8 exist (uniform)
-      float* mo = dmp_o + cw * 16 * D;
+      // rows normalised by their sums, into this warp's row-major dump
+      const float inv0 = lt0 > 0.f ? __fdividef(1.f, lt0) : 0.f;
+      const float inv1 = lt1 > 0.f ? __fdividef(1.f, lt1) : 0.f;
+      uint8_t* mo = dmp_o + cw * C::kDumpWarpBytes;
+      if constexpr (!kFp8) {
+        // fragment element e of n-tile n: column 8n + 2cq + (e & 1)
 #pragma unroll
-      for (int n = 0; n < C::kOTiles; ++n) {
-        mo[(n * 4 + 0) * 32 + lane] = o[n][0];
-        mo[(n * 4 + 1) * 32 + lane] = o[n][1];
-        if (hi_rows) {
-          mo[(n * 4 + 2) * 32 + lane] = o[n][2];
-          mo[(n * 4 + 3) * 32 + lane] = o[n][3];
+        for (int n = 0; n < C::kOTiles; ++n) {
+          const int c = 2 * n + (cq >> 1), off = (cq & 1) * 8;
+          *reinterpret_cast<float2*>(
+              mo + dump_off<C::kDumpRowBytes>(r, c) + off) =
+              make_float2(o[n][0] * inv0, o[n][1] * inv0);
+          if (hi_rows)
+            *reinterpret_cast<float2*>(
+                mo + dump_off<C::kDumpRowBytes>(r + 8, c) + off) =
+                make_float2(o[n][2] * inv1, o[n][3] * inv1);
+        }
+      } else {
+        // permuted columns: element e of n-tile n is column
+        // (2cq + (e & 1)) * D/8 + n, so n-tiles 8c' .. 8c'+7 fill one chunk
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e >= 2 && !hi_rows) break;
+          const float inv = e < 2 ? inv0 : inv1;
+#pragma unroll
+          for (int ng = 0; ng < D / 64; ++ng) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __half2 h = __floats2half2_rn(o[8 * ng + 2 * i][e] * inv,
+                                                  o[8 * ng + 2 * i + 1][e] * inv);
+              memcpy(&wv[i], &h, 4);
+            }
+            const int c = (2 * cq + (e & 1)) * (D / 64) + ng;
+            *reinterpret_cast<uint4*>(
+                mo + dump_off<C::kDumpRowBytes>(r + 8 * (e >> 1), c)) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
         }
       }
       if (cq == 0) {
@@ -1316,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;  // g == t1 - 1: the block's range is done
       }
     }
-    par ^= 1;
+    if (++par == C::kGroups) par = 0;
     if (++stage == C::kStages) {
       stage = 0;
       ph ^= 1u;

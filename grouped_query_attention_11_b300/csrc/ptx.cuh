@@ -65,18 +65,35 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep until the phase
+// completes or about `hint_ns` nanoseconds pass, issuing nothing meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar,
+                                                    uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // after `limit_ns` nanoseconds of wall time and returns false, so that no
-// wait in these kernels can spin forever.
+// wait in these kernels can spin forever.  A waiting warp sleeps in its
+// try_wait instead of polling, leaving the issue slots of its SM
+// sub-partition to the warps that compute.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar,
                                                   uint32_t parity,
                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++n & 255u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
