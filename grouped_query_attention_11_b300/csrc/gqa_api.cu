@@ -99,9 +99,20 @@ struct Variant {
   int smem;
 };
 
-template <int KV, bool QB, int D, int HB, bool PG>
+template <int KV, bool QB, int D, int HB, bool PG, bool NR = false>
 Variant variant() {
-  return {&gqa_decode_kernel<KV, QB, D, HB, PG>, Cfg<KV, D, HB>::kSmemBytes};
+  return {&gqa_decode_kernel<KV, QB, D, HB, PG, NR>,
+          Cfg<KV, D, HB, NR>::kSmemBytes};
+}
+
+// 8-bit caches whose units have at most 8 query rows: the narrow-row path.
+template <int KV>
+Variant pick_nr(bool q_bf16, int D) {
+  if (D == 64)
+    return q_bf16 ? variant<KV, true, 64, 1, false, true>()
+                  : variant<KV, false, 64, 1, false, true>();
+  return q_bf16 ? variant<KV, true, 128, 1, false, true>()
+                : variant<KV, false, 128, 1, false, true>();
 }
 
 template <int KV, bool QB, int D, bool PG>
@@ -118,8 +129,12 @@ Variant pick_d(int D, int hb) {
   return D == 64 ? pick_hb<KV, QB, 64, PG>(hb) : pick_hb<KV, QB, 128, PG>(hb);
 }
 
-// Paged caches are instantiated for the 16-bit element types.
-Variant pick(int kv, bool q_bf16, int D, int hb, bool paged = false) {
+// Paged caches are instantiated for the 16-bit element types.  rows: query
+// rows per unit (R).
+Variant pick(int kv, bool q_bf16, int D, int hb, int rows, bool paged = false) {
+  if (is_fp8(kv) && rows <= 8)
+    return kv == kKvE5M2 ? pick_nr<kKvE5M2>(q_bf16, D)
+                         : pick_nr<kKvE4M3>(q_bf16, D);
   if (paged)
     return kv == kKvBF16 ? pick_d<kKvBF16, true, true>(D, hb)
                          : pick_d<kKvF16, false, true>(D, hb);
@@ -293,7 +308,7 @@ gqa_status launch(const void* q, const void* k, const void* v,
   const long long units = static_cast<long long>(B) * Hkv * NHC;
   if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
 
-  const Variant var = pick(kv_kind, q_bf16, D, hb, paged);
+  const Variant var = pick(kv_kind, q_bf16, D, hb, R, paged);
   const int elem_bytes = is_fp8(kv_kind) ? 1 : 2;
   // the TMA view [planes][rows][D]: (B*Hkv, Smax) or (num_pages*Hkv,
   // page_size)
@@ -427,7 +442,7 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
   const long long units = static_cast<long long>(B) * Hkv * NHC;
   if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
 
-  const Variant var = pick(kv_kind, q_bf16, D, hb);
+  const Variant var = pick(kv_kind, q_bf16, D, hb, R);
   CUtensorMap map_k, map_v;
   if (!make_cache_map(&map_k, k, 2, B, Hkv, Smax, D) ||
       !make_cache_map(&map_v, v, 2, B, Hkv, Smax, D))

@@ -139,7 +139,11 @@ struct DecodeParams {
 
 // ------------------------------------------------------------ compile-time
 
-template <int KV, int D, int HB>
+// NR: the narrow-row path for 8-bit caches whose units have at most 8 query
+// rows.  Keys are the 16-row A operand and the group's rows the 8 columns of
+// each mma (S^T = K Q^T, O^T = V^T P^T), which halves the mma work of the
+// 16-row padding and the O registers.
+template <int KV, int D, int HB, bool NR = false>
 struct Cfg {
   static constexpr int kElemBytes = is_fp8(KV) ? 1 : 2;
   static constexpr int kRowBytes = D * kElemBytes;            // one token
@@ -162,6 +166,9 @@ struct Cfg {
   static constexpr int kPSteps = kWarpTokens / 16;  // PV k-steps per warp
   static constexpr int kOTiles = D / 8;             // O n-tiles
   static constexpr int kQSteps = D / 16;            // QK k-steps
+  static constexpr int kMTiles = kWarpTokens / 16;  // NR: key m-tiles per warp
+  // mma accumulator tiles of O per warp: O n-tiles, or (NR) O^T m-tiles
+  static constexpr int kOAcc = NR ? D / 16 : D / 8;
   static constexpr int kRowsPad = HB * 16;
   // Unit dump: per consumer warp its 16 rows of normalised O, row-major, in
   // f16 for the 8-bit caches (values bounded by the code range) and fp32
@@ -184,6 +191,8 @@ struct Cfg {
   static_assert(kStages >= 2 * kGroups && kStages % kGroups == 0,
                 "pipeline needs two stages per group");
   static_assert(kWarpsPerBlock >= 1, "a head block needs a warp per group");
+  static_assert(!NR || (is_fp8(KV) && HB == 1 && kMTiles >= 1),
+                "the narrow-row path serves 8-bit caches with one head block");
   static_assert(kSTiles % 2 == 0 && kPSteps >= 1, "warp tile shape");
   static_assert(kQSteps % 2 == 0, "QK k-steps are split into two chains");
   // Short accumulator chains: with few S tiles per warp the QK k-loop is
@@ -427,6 +436,23 @@ __device__ __forceinline__ uint32_t fp8_hi(uint32_t w) {
     return __byte_perm(w, 0u, 0x3424);
   } else {
     return ptx::e4m3x2_to_f16x2(w >> 16);
+  }
+}
+
+// 8-bit cache: the K bytes of token row t (in the tile) that thread column cq
+// owns, d in [cq*D/4, (cq+1)*D/4): word ks holds d = cq*D/4 + 4ks + {0..3},
+// i.e. the k slots (2cq, 2cq+1) and (2cq+8, 2cq+9) of QK k-step ks.
+template <int D>
+__device__ __forceinline__ void fp8_key_words(uint32_t kbase, int t, int cq,
+                                              uint32_t (&kw)[D / 16]) {
+  if constexpr (D == 128) {
+    const uint4 a = ptx::lds128(kbase + swz8<D>(t, 2 * cq));
+    const uint4 b = ptx::lds128(kbase + swz8<D>(t, 2 * cq + 1));
+    kw[0] = a.x; kw[1] = a.y; kw[2] = a.z; kw[3] = a.w;
+    kw[4] = b.x; kw[5] = b.y; kw[6] = b.z; kw[7] = b.w;
+  } else {
+    const uint4 a = ptx::lds128(kbase + swz8<D>(t, cq));
+    kw[0] = a.x; kw[1] = a.y; kw[2] = a.z; kw[3] = a.w;
   }
 }
 
@@ -683,12 +709,12 @@ __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
   }
 }
 
-template <int KV, bool QBF16, int D, int HB, bool PAGED>
+template <int KV, bool QBF16, int D, int HB, bool PAGED, bool NR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v,
                       const DecodeParams p) {
-  using C = Cfg<KV, D, HB>;
+  using C = Cfg<KV, D, HB, NR>;
   constexpr bool kFp8 = is_fp8(KV);
   constexpr bool kMmaBF16 = !kFp8 && QBF16;
   using QT = typename std::conditional<QBF16, __nv_bfloat16, __half>::type;
@@ -960,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   TileWalk w = w0;
   uint32_t qf[C::kQSteps][4];
-  float o[C::kOTiles][4];
+  float o[C::kOAcc][4];
   float m[2], l[2];
   float s_mult = 0.f, o_mult = 1.f;
   bool fresh = true;
@@ -1006,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         o_mult = __ldg(p.v_scale + sidx);
       }
 #pragma unroll
-      for (int n = 0; n < C::kOTiles; ++n)
+      for (int n = 0; n < C::kOAcc; ++n)
         o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
       m[0] = m[1] = -INFINITY;
       l[0] = l[1] = 0.f;
@@ -1032,6 +1058,141 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool tail = (w.ti == w.nt - 1) ||
                       (w.ti * kTileTokens + kTileTokens - 1 > L - T);
 
+    if constexpr (NR) {
+    // ==== narrow rows: S^T = K Q^T, O^T += V^T P^T (keys / d on the mma
+    // rows, this unit's <= 8 query rows on its 8 columns) ====
+    // S^T m-tile mt: tokens trow0 + 16mt + r (+8) on the rows, query rows
+    // 2cq, 2cq+1 on the columns: entries 0/1 (token r), 2/3 (token r + 8).
+    float st[C::kMTiles][4];
+#pragma unroll
+    for (int mt = 0; mt < C::kMTiles; ++mt) {
+      uint32_t ka[D / 16], kb[D / 16];
+      fp8_key_words<D>(kbase, trow0 + mt * 16 + r, cq, ka);
+      fp8_key_words<D>(kbase, trow0 + mt * 16 + r + 8, cq, kb);
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < C::kQSteps; ++ks) {
+        // A: keys (rows r, r+8) at the k slots of q's permuted d (B: row r)
+        const uint32_t a[4] = {fp8_lo<KV>(ka[ks]), fp8_lo<KV>(kb[ks]),
+                               fp8_hi<KV>(ka[ks]), fp8_hi<KV>(kb[ks])};
+        if (ks & 1)
+          ptx::mma16816<false>(sb, a, qf[ks][0], qf[ks][2]);
+        else
+          ptx::mma16816<false>(sa, a, qf[ks][0], qf[ks][2]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st[mt][e] = sa[e] + sb[e];
+    }
+    // online softmax of rows 2cq (entries 0, 2) and 2cq+1 (entries 1, 3);
+    // a column's 8 lanes (r = 0..7) reduce with three shuffles
+    {
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float v = st[mt][e] * s_mult;
+          if (tail && tok0 + mt * 16 + r + 8 * (e >> 1) > lim0) v = -INFINITY;
+          st[mt][e] = v;
+        }
+        mx0 = fmaxf(mx0, fmaxf(st[mt][0], st[mt][2]));
+        mx1 = fmaxf(mx1, fmaxf(st[mt][1], st[mt][3]));
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float al0 = ptx::ex2(m[0] - base0);
+      const float al1 = ptx::ex2(m[1] - base1);
+      m[0] = mn0;
+      m[1] = mn1;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) {
+        st[mt][0] = ptx::ex2(st[mt][0] - base0);
+        st[mt][2] = ptx::ex2(st[mt][2] - base0);
+        st[mt][1] = ptx::ex2(st[mt][1] - base1);
+        st[mt][3] = ptx::ex2(st[mt][3] - base1);
+        rs0 += st[mt][0] + st[mt][2];
+        rs1 += st[mt][1] + st[mt][3];
+      }
+      l[0] = l[0] * al0 + rs0;
+      l[1] = l[1] * al1 + rs1;
+      if (al0 != 1.f || al1 != 1.f) {
+#pragma unroll
+        for (int n = 0; n < C::kOAcc; ++n) {
+          o[n][0] *= al0;
+          o[n][2] *= al0;
+          o[n][1] *= al1;
+          o[n][3] *= al1;
+        }
+      }
+    }
+    // O^T m-tile mt_d holds d = (D/8) r + 2 mt_d (rows r) and + 1 (rows
+    // r + 8): each thread row owns one contiguous run of D/8 V bytes.
+#pragma unroll
+    for (int kk = 0; kk < C::kMTiles; ++kk) {
+      // P^T as the B operand: the (token x row) 8x8 blocks transposed
+      const uint32_t b0 =
+          ptx::movmatrix_trans(ptx::pack2<false>(st[kk][0], st[kk][1]));
+      const uint32_t b1 =
+          ptx::movmatrix_trans(ptx::pack2<false>(st[kk][2], st[kk][3]));
+      const int tk = tok0 + kk * 16 + 2 * cq;  // tokens tk, tk+1, tk+8, tk+9
+      const int ta = trow0 + kk * 16 + 2 * cq;
+      constexpr int kW = D / 32;  // 32-bit words per thread per token row
+      uint32_t xa[kW], xb[kW], xc[kW], xd[kW];
+      if constexpr (D == 128) {
+        const uint4 a = ptx::lds128(vbase + swz8<D>(ta, r));
+        const uint4 b = ptx::lds128(vbase + swz8<D>(ta + 1, r));
+        const uint4 c = ptx::lds128(vbase + swz8<D>(ta + 8, r));
+        const uint4 d = ptx::lds128(vbase + swz8<D>(ta + 9, r));
+        xa[0] = a.x; xa[1] = a.y; xa[2] = a.z; xa[3] = a.w;
+        xb[0] = b.x; xb[1] = b.y; xb[2] = b.z; xb[3] = b.w;
+        xc[0] = c.x; xc[1] = c.y; xc[2] = c.z; xc[3] = c.w;
+        xd[0] = d.x; xd[1] = d.y; xd[2] = d.z; xd[3] = d.w;
+      } else {
+        const int half = (r & 1) * 8;
+        const uint2 a = ptx::lds64(vbase + swz8<D>(ta, r >> 1) + half);
+        const uint2 b = ptx::lds64(vbase + swz8<D>(ta + 1, r >> 1) + half);
+        const uint2 c = ptx::lds64(vbase + swz8<D>(ta + 8, r >> 1) + half);
+        const uint2 d = ptx::lds64(vbase + swz8<D>(ta + 9, r >> 1) + half);
+        xa[0] = a.x; xa[1] = a.y;
+        xb[0] = b.x; xb[1] = b.y;
+        xc[0] = c.x; xc[1] = c.y;
+        xd[0] = d.x; xd[1] = d.y;
+      }
+      if (tail) {  // bytes of tokens past the end may hold anything
+        const uint32_t ka = tk < L ? ~0u : 0u, kb = tk + 1 < L ? ~0u : 0u;
+        const uint32_t kc = tk + 8 < L ? ~0u : 0u, kd = tk + 9 < L ? ~0u : 0u;
+#pragma unroll
+        for (int i = 0; i < kW; ++i) {
+          xa[i] &= ka;
+          xb[i] &= kb;
+          xc[i] &= kc;
+          xd[i] &= kd;
+        }
+      }
+#pragma unroll
+      for (int wi = 0; wi < kW; ++wi) {
+        // byte j of word wi: d = (D/8) r + 4wi + j -> m-tile 2wi + j/2, row
+        // r + 8 (j & 1); pair up tokens (tk, tk+1) and (tk+8, tk+9)
+        const uint32_t p01 = __byte_perm(xa[wi], xb[wi], 0x5140);
+        const uint32_t p23 = __byte_perm(xa[wi], xb[wi], 0x7362);
+        const uint32_t q01 = __byte_perm(xc[wi], xd[wi], 0x5140);
+        const uint32_t q23 = __byte_perm(xc[wi], xd[wi], 0x7362);
+        const uint32_t a0[4] = {fp8_lo<KV>(p01), fp8_hi<KV>(p01),
+                                fp8_lo<KV>(q01), fp8_hi<KV>(q01)};
+        const uint32_t a1[4] = {fp8_lo<KV>(p23), fp8_hi<KV>(p23),
+                                fp8_lo<KV>(q23), fp8_hi<KV>(q23)};
+        ptx::mma16816<false>(o[2 * wi], a0, b0, b1);
+        ptx::mma16816<false>(o[2 * wi + 1], a1, b0, b1);
+      }
+    }
+    } else {
     // ---- S = Q K^T for this warp's tokens ----
     float s[C::kSTiles][4];
     float s2[C::kSplitQK ? C::kSTiles : 1][4];  // odd k-steps when split
@@ -1065,15 +1226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; n < C::kSTiles; ++n) {
         const int t = trow0 + n * 8 + r;
         uint32_t kw[D / 16];
-        if constexpr (D == 128) {
-          const uint4 a = ptx::lds128(kbase + swz8<D>(t, 2 * cq));
-          const uint4 b = ptx::lds128(kbase + swz8<D>(t, 2 * cq + 1));
-          kw[0] = a.x; kw[1] = a.y; kw[2] = a.z; kw[3] = a.w;
-          kw[4] = b.x; kw[5] = b.y; kw[6] = b.z; kw[7] = b.w;
-        } else {
-          const uint4 a = ptx::lds128(kbase + swz8<D>(t, cq));
-          kw[0] = a.x; kw[1] = a.y; kw[2] = a.z; kw[3] = a.w;
-        }
+        fp8_key_words<D>(kbase, t, cq, kw);
 #pragma unroll
         for (int ks = 0; ks < C::kQSteps; ++ks) {
           const uint32_t b0 = fp8_lo<KV>(kw[ks]);
@@ -1253,6 +1406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
+    }  // NR / wide rows
+
     // ---- release the stage ----
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&empty[stage]);
@@ -1269,6 +1424,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_abort = 1;
       }
       dph ^= 1u;
+      uint8_t* mo = dmp_o + cw * C::kDumpWarpBytes;
+      if constexpr (NR) {
+        // rows 2cq, 2cq+1: sums over the column's 8 lanes; this thread's run
+        // d = (D/8) r + j of each row holds O^T entries 0 / 1 (j even) and
+        // 2 / 3 (j odd) of m-tile j / 2
+        float lt0 = l[0], lt1 = l[1];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+          lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+        }
+        const float inv0 = lt0 > 0.f ? __fdividef(1.f, lt0) : 0.f;
+        const float inv1 = lt1 > 0.f ? __fdividef(1.f, lt1) : 0.f;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t w0[4], w1[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 h0 = __floats2half2_rn(o[4 * h + i][0] * inv0,
+                                                 o[4 * h + i][2] * inv0);
+            const __half2 h1 = __floats2half2_rn(o[4 * h + i][1] * inv1,
+                                                 o[4 * h + i][3] * inv1);
+            memcpy(&w0[i], &h0, 4);
+            memcpy(&w1[i], &h1, 4);
+          }
+          const int c = r * (D / 64) + h;
+          if (2 * cq < p.R)
+            *reinterpret_cast<uint4*>(
+                mo + dump_off<C::kDumpRowBytes>(2 * cq, c)) =
+                make_uint4(w0[0], w0[1], w0[2], w0[3]);
+          if (2 * cq + 1 < p.R)
+            *reinterpret_cast<uint4*>(
+                mo + dump_off<C::kDumpRowBytes>(2 * cq + 1, c)) =
+                make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        }
+        if (r == 0) {
+          dmp_m[cw * 16 + 2 * cq] = m[0];
+          dmp_m[cw * 16 + 2 * cq + 1] = m[1];
+          dmp_l[cw * 16 + 2 * cq] = lt0;
+          dmp_l[cw * 16 + 2 * cq + 1] = lt1;
+        }
+      } else {
       float lt0 = l[0], lt1 = l[1];
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 1);
       lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
@@ -1278,7 +1475,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // rows normalised by their sums, into this warp's row-major dump
       const float inv0 = lt0 > 0.f ? __fdividef(1.f, lt0) : 0.f;
       const float inv1 = lt1 > 0.f ? __fdividef(1.f, lt1) : 0.f;
-      uint8_t* mo = dmp_o + cw * C::kDumpWarpBytes;
       if constexpr (!kFp8) {
         // fragment element e of n-tile n: column 8n + 2cq + (e & 1)
 #pragma unroll
@@ -1321,6 +1517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dmp_l[cw * 16 + r] = lt0;
         dmp_l[cw * 16 + r + 8] = lt1;
       }
+      }  // NR / wide rows
       const bool last = (g == t1 - 1);
       const long long us = w.pref + static_cast<long long>(w.j) * w.nt;
       const int u = w.b * HU + w.j;

@@ -58,6 +58,13 @@ CASES = [
      ("list", 400, 1, 70, 333)),
     ("e5m2_g8_d64_f16", 2, 16, 2, 64, 300, "f16", "e5m2", ("list", 300, 129)),
     ("e5m2_mqa_g64", 1, 64, 1, 128, 200, "bf16", "e5m2", ("uniform",)),
+    # 8-bit caches with 9..16 rows per unit: the wide one-head-block path
+    # (groups of <= 8 rows take the narrow-row path)
+    ("fp8_g16_d128_wide", 2, 32, 2, 128, 300, "bf16", "e4m3",
+     ("list", 300, 77)),
+    ("e5m2_g12_d64_wide", 2, 24, 2, 64, 200, "f16", "e5m2", ("list", 130, 200)),
+    ("fp8_g2_d128_narrow", 3, 8, 4, 128, 333, "bf16", "e4m3",
+     ("list", 333, 1, 64)),
     # more sequences than threads per block: the general scheduler prologue
     ("bf16_many_sequences", 300, 8, 2, 64, 70, "bf16", "same",
      ("ragged", 0, 70)),
