@@ -51,14 +51,41 @@ KERNEL_SOURCES = ("gqa_decode_kernel.cuh", "ptx.cuh", "gqa_api.cu")
 GRAPH_STEPS = 100  # steps per captured CUDA graph (--graph, --op append)
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace runs collapsed, so
+    that an edit of comments or layout leaves the hash unchanged (string and
+    character literals are kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sources_sha256() -> str:
-    """Hash of the CUDA sources the profiled kernel was built from."""
+    """Hash of the CUDA sources the profiled kernel was built from (their
+    code only: comments and whitespace do not count)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "grouped_query_attention_11_b300", "csrc")
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -724,10 +724,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  // Dump area of the unit epilogue: per consumer warp its O fragments
-  // (position (n*4 + e)*32 + lane), row maxima and row sums.
+  // Dump area of the unit epilogue: per consumer warp its 16 normalised O
+  // rows (row-major, chunks swizzled as in dump_off), then the row maxima and
+  // row sums of all warps.
   uint8_t* dmp_o = ring + C::kRingBytes;
-  float* dmp_m = reinterpret_cast<float*>(dmp_o + kConsumerWarps * C::kDumpWarpBytes);
+  float* dmp_m =
+      reinterpret_cast<float*>(dmp_o + kConsumerWarps * C::kDumpWarpBytes);
   float* dmp_l = dmp_m + kConsumerWarps * 16;
   uint64_t* full = reinterpret_cast<uint64_t*>(dmp_l + kConsumerWarps * 16);
   uint64_t* empty = full + C::kStages;
