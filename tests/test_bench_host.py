@@ -1,0 +1,82 @@
+"""Host-side checks of bench.py (no GPU): the source hash that ties profiled
+DRAM traffic to the kernel code, and the JSON line of the reference arm (the
+CPU oracle), which runs anywhere."""
+import json
+import os
+import shutil
+import subprocess
+import sys
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_code_only_drops_comments_and_layout():
+    a = 'int x = 1;  // one\n/* block\n comment */ float y;\n'
+    b = 'int x = 1;\nfloat   y;'
+    assert bench._code_only(a) == bench._code_only(b)
+    # literals survive, including comment markers and quotes inside them
+    s = 'const char* p = "a//b /*c*/"; char q = \'"\';'
+    assert bench._code_only(s) == s
+    # a code change does not
+    assert bench._code_only("int x = 1;") != bench._code_only("int x = 2;")
+
+
+def _fake_root(tmp_path, traffic, sha):
+    csrc = tmp_path / "grouped_query_attention_11_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in bench.KERNEL_SOURCES:
+        shutil.copy(os.path.join(ROOT, "grouped_query_attention_11_b300",
+                                 "csrc", name), csrc / name)
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "gqa_decode_kernel__w.md").write_text(
+        "# summary\n\n"
+        f"- traffic_bytes_per_launch: `{traffic}`\n"
+        f"- kernel_sources_sha256: `{sha}`\n")
+    return str(tmp_path)
+
+
+def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    sha = bench.kernel_sources_sha256()
+    monkeypatch.setattr(bench, "ROOT", _fake_root(tmp_path, 12345, sha))
+    assert bench.kernel_sources_sha256() == sha
+    assert bench.profiled_traffic("w") == 12345
+    assert bench.profiled_traffic("missing") is None
+    # a comment added to a kernel source keeps the summary valid ...
+    src = tmp_path / "grouped_query_attention_11_b300" / "csrc" / \
+        bench.KERNEL_SOURCES[0]
+    src.write_text(src.read_text() + "\n// a note\n")
+    assert bench.profiled_traffic("w") == 12345
+    # ... a code change does not
+    src.write_text(src.read_text() + "\nstatic int changed = 1;\n")
+    assert bench.profiled_traffic("w") is None
+
+
+def test_reference_arm_json_line():
+    out = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl",
+         "reference", "--workload", "tiny_b1_h8_kv2_d64_s128_f16", "--steps",
+         "2", "--warmup", "3"],
+        capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup",
+              "ms_per_step", "higher_is_better", "scaling", "vs_baseline",
+              "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference"
+    assert d["warmup"] >= 3
+    assert d["higher_is_better"] is False
+    assert d["value"] > 0 and d["unit"] == "us/step"
+    assert d["config"]["workload"] == "tiny_b1_h8_kv2_d64_s128_f16"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
