@@ -882,6 +882,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long g = t0; g < t1; ++g, ++it) {
         const int stage = static_cast<int>(it % C::kStages);
         const uint32_t ph = static_cast<uint32_t>((it / C::kStages) & 1);
+        const int kvh = w.j / p.NHC;
+        const int tok = w.ti * kTileTokens;
+        // paged: the tile's block-table entry is loaded before the wait for
+        // its ring slot, so that the load's latency hides behind the wait
+        // (a tile lies inside one page: page_size is a multiple of it)
+        int pg = 0;
+        if constexpr (PAGED)
+          pg = __ldg(p.block_table + static_cast<size_t>(w.b) * p.max_pages +
+                     tok / p.page_size);
         if (!ptx::mbar_wait_bounded(&empty[stage], ph ^ 1u, kWaitLimitNs)) {
           atomicOr(p.error, kErrWaitTimeout);
           s_abort = 1;
@@ -889,15 +898,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (s_abort) break;
         ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-        const int kvh = w.j / p.NHC;
-        const int tok = w.ti * kTileTokens;
         // tile coordinates in the cache view [planes][tokens][D]
         int row = tok, plane = w.b * p.Hkv + kvh;
         if constexpr (PAGED) {
-          // a tile lies inside one page (page_size is a multiple of it)
-          int pg = __ldg(p.block_table +
-                         static_cast<size_t>(w.b) * p.max_pages +
-                         tok / p.page_size);
           if (pg < 0 || pg >= p.num_pages) {
             atomicOr(p.error, kErrBadPage);
             pg = 0;
