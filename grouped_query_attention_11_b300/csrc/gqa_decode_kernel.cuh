@@ -89,7 +89,7 @@ constexpr int kRegsBig = 224;
 static_assert(128 * kRegsSmall + 256 * kRegsBig <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int kMaxUnitRows = 64;  // query heads per unit (4 head blocks)
-constexpr int kPrefetchTiles = 2; // tiles per block warmed in L2 at launch
+constexpr int kPrefetchTiles = 12; // tiles per block warmed in L2 at launch
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
 // Dynamic shared memory per block: the sm_100-family opt-in maximum (227 KB)
