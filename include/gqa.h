@@ -261,15 +261,19 @@ const char* gqa_status_string(gqa_status status);
  * fault flags the kernels raised on it since the last query: 0 when none.
  * Bit 0: a pipeline wait gave up after its time limit (the affected outputs
  * are unspecified).  Bit 1: a paged call met a block-table entry outside
- * [0, num_pages).  Bit 2: an append found a sequence's cache full.  Returns GQA_ERR_CUDA if the synchronisation fails.
+ * [0, num_pages).  Bit 2: an append found a sequence's cache full.
+ * Returns GQA_ERR_CUDA if the synchronisation fails.
  */
 gqa_status gqa_device_errors(void* stream, uint32_t* flags);
 
 /*
  * gqa_set_num_ctas — test and tuning hook: fixes the number of persistent
- * thread blocks the decode kernels launch (0 restores the default, one full
- * wave of the device).  It changes how the sequence axis is split between
- * blocks, never the result beyond fp32 rounding.  Process-wide; host only.
+ * thread blocks the decode kernels launch and makes all of them take part
+ * (0 restores the default: one full wave of the device, of which a batch
+ * whose sequences all have the same number of 64-token tiles may use a
+ * smaller, unit-aligned count).  It changes how the sequence axis is split
+ * between blocks, never the result beyond fp32 rounding.  Process-wide; host
+ * only.
  */
 void gqa_set_num_ctas(int num_ctas);
 
