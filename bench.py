@@ -326,6 +326,19 @@ def bench_append(a, w, name, peak, peak_kind):
     return 0
 
 
+def job_us_per_step(us: float, ws: int, device) -> float:
+    """Whole-job time per step of ws replicas that each ran the same steps:
+    the slowest rank's time (max over ranks, one all-reduce on the timing
+    only) divided by the ws steps the job completed in it."""
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([us], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us = float(t.item())
+    return us / ws
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -452,15 +465,8 @@ def main(argv=None):
     assert gq.gqa_device_errors(stream) == 0
 
     us = ev0.elapsed_time(ev1) * 1e3 / K
-    if ws > 1:
-        # replicas: every rank ran K steps; the job's time is the slowest
-        # rank's, and it processed ws steps per step-time
-        t = torch.tensor([us], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        us_max = float(t.item())
-    else:
-        us_max = us
-    job_us_per_step = us_max / ws
+    # replicas: every rank ran K steps; the job's time is the slowest rank's
+    job_us = job_us_per_step(us, ws, dev)
 
     # ---- end to end through the public API, host buffers ----
     e2e = None
@@ -491,11 +497,8 @@ def main(argv=None):
     ee.record(stream)
     torch.cuda.synchronize()
     e2e_us = es.elapsed_time(ee) * 1e3 / ek
-    if ws > 1:
-        t = torch.tensor([e2e_us], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_us = float(t.item())
-    e2e = {"value": e2e_us / ws, "unit": "us/step", "h2d_bytes_per_step": h2d,
+    e2e = {"value": job_us_per_step(e2e_us, ws, dev), "unit": "us/step",
+           "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": ek}
     del dd
 
@@ -511,9 +514,9 @@ def main(argv=None):
     if not a.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, inp, budget_s=10.0)
     line = {
-        "metric": METRIC, "value": job_us_per_step, "unit": "us/step",
+        "metric": METRIC, "value": job_us, "unit": "us/step",
         "n_gpus": ws, "steps": K, "warmup": warmup,
-        "ms_per_step": job_us_per_step / 1e3, "higher_is_better": False,
+        "ms_per_step": job_us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if
         w.kv == "same" else f"{w.kv} KV / {w.dtype} q,out", "data": "synthetic",
         "config": cfg,
