@@ -137,6 +137,23 @@ def test_split_invariance_fp8(oracle_mod):
         assert_contract(out, ref, f"fp8 ctas={n}")
 
 
+@pytest.mark.parametrize("kv", ["e4m3", "e5m2"])
+def test_fp8_per_tensor_scales(oracle_mod, kv):
+    """One scale for each whole tensor (K, V): every (sequence, KV head)
+    entry set to the tensor's largest.  Both sides dequantise code x scale,
+    so parity holds whatever the scales; the largest keeps values O(1)."""
+    w = Workload("per_tensor_" + kv, 3, 32, 8, 128, 400, "bf16", kv=kv,
+                 lens=("list", 400, 3, 200), seed=33)
+    inp = make_inputs(w, pad="nan")
+    inp["k_scale"] = torch.full_like(inp["k_scale"],
+                                     float(inp["k_scale"].max()))
+    inp["v_scale"] = torch.full_like(inp["v_scale"],
+                                     float(inp["v_scale"].max()))
+    out = run_cuda(inp)
+    ref = oracle_full(oracle_mod, inp)
+    assert_close(out, ref, w.name)
+
+
 def test_deterministic_bitwise():
     w = Workload("det", 4, 64, 8, 128, 800, "bf16", lens=("ragged", 1, 800),
                  seed=33)
