@@ -16,12 +16,17 @@
 //  * Persistent blocks.  The grid is one wave of blocks; block c takes the
 //    contiguous tile range [c*N/P, (c+1)*N/P).  Every block streams the same
 //    number of KV bytes (+-1 tile), whatever the length mix.  A unit cut by a
-//    range boundary is finished by the fused split combine below.
+//    range boundary is finished by the fused split combine below.  When all
+//    sequences have the same tile count, P is a host-chosen count that puts
+//    the range boundaries on unit boundaries (see DecodeParams::p_align).
 //  * Warp roles.  A block is three warpgroups.  Warpgroup 0: one producer
 //    warp and three merge warps; warpgroups 1 and 2: eight consumer warps.
-//    setmaxnreg moves registers from warpgroup 0 (56 per
-//    thread) to the consumers (224), whose mma fragments, accumulators and
-//    query rows then never spill.
+//    setmaxnreg moves registers from warpgroup 0 (56 per thread) to the
+//    consumers (224) for their mma fragments, accumulators and query rows.
+//  * Launch overlap.  Launched as a programmatic dependent: before
+//    griddepcontrol.wait a block only initialises barriers and asks L2 for
+//    its first tiles (cp.async.bulk.prefetch.tensor), which overlaps the
+//    previous kernel's last blocks; every global read comes after the wait.
 //  * KV stream.  The producer warp issues TMA tensor loads (128-byte
 //    swizzle, L2 evict-first) of the K and V tiles into a multi-stage shared
 //    memory ring guarded by mbarriers.  Each KV byte is read from HBM once and
@@ -30,23 +35,25 @@
 //    A fragments (16 rows per head block; G < 16 pads with zero rows) and run
 //    QK^T and PV through mma.sync m16n8k16 with fp32 accumulation.  The online
 //    softmax (running row max, rescale, row sum) lives in registers; row
-//    reductions are two quad shuffles.
+//    reductions are two quad shuffles.  Narrow rows (NR: 8-bit caches with at
+//    most 8 query rows a unit) swap the operands: keys and head dimensions
+//    on the mma rows, the unit's rows on its 8 columns (S^T = K Q^T, O^T +=
+//    V^T P^T with P^T from movmatrix), halving the padded mma work.
 //  * Consumer groups.  The consumer warps form groups (two of four warps, or
 //    four of two for the 8-bit caches with one head block) that take the
 //    ring's stages in turn, each with its own softmax state, so that one
 //    group's dependent mma / exp chains overlap the others'.
 //  * Asynchronous unit epilogue.  At the end of a unit every consumer warp
 //    only dumps its softmax state to shared memory (its rows normalised,
-//    row-major) and
-//    signals an mbarrier; it goes straight on with the next unit, whose query
-//    rows it has already started loading.  The merge warps combine the eight
+//    row-major) and signals an mbarrier; it goes straight on with the next
+//    unit, whose query rows it has already started loading.  The merge warps combine the eight
 //    states, write the output rows or a split partial, and publish the
 //    block's arrival, off the consumers' critical path.
 //  * FP8 cache (E4M3 or E5M2).  Bytes are turned into exact f16 pairs in
 //    registers (cvt.rn.f16x2.e4m3x2; an E5M2 byte is the upper byte of its
-//    f16); q is moved into f16 with a per-head-block power
-//    of two so no value can overflow; k_scale and the power of two fold into
-//    the score multiplier and v_scale into the output.
+//    f16); q is moved into f16 with a per-warp power of two so no value can
+//    overflow; k_scale and the power of two fold into the score multiplier
+//    and v_scale into the output.
 //  * Split combine.  A unit covered by one block is written out directly;
 //    otherwise each block writes a normalised partial (O, log2-sum-exp) and
 //    bumps a per-unit counter; the block that arrives last merges all
