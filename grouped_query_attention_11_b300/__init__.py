@@ -21,7 +21,7 @@ its names:
   any device allocation;
 * :func:`gqa_kv_bytes_per_token`, :func:`gqa_status_string`,
   :func:`gqa_device_errors`, :func:`gqa_set_num_ctas`,
-  :func:`gqa_last_launch_count`.
+  :func:`gqa_set_wait_limit_ns`, :func:`gqa_last_launch_count`.
 """
 from __future__ import annotations
 
@@ -56,6 +56,7 @@ SIGNATURES = {
     "gqa_status_string": (ctypes.c_char_p, [_I32]),
     "gqa_device_errors": (_I32, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_set_num_ctas": (None, [_I32]),
+    "gqa_set_wait_limit_ns": (None, [ctypes.c_longlong]),
     "gqa_last_launch_count": (_I32, []),
 }
 
@@ -97,6 +98,12 @@ def gqa_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
 
 def gqa_set_num_ctas(n: int) -> None:
     lib().gqa_set_num_ctas(int(n))
+
+
+def gqa_set_wait_limit_ns(ns: int) -> None:
+    """Test hook: time limit of the kernels' pipeline waits (0: give up at the
+    first wait that is not already complete; negative: the default)."""
+    lib().gqa_set_wait_limit_ns(int(ns))
 
 
 def gqa_last_launch_count() -> int:
@@ -151,6 +158,39 @@ def _check_dev(name, t):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_layout(q, k, v, seq_lens, out, *, chunk=False, paged=False,
+                  scales=None):
+    """Shape / dtype / device agreement of a decode call's tensors, checked
+    before the C call: the library sizes every device access from q's and
+    k_cache's dimensions, so a smaller v_cache, out, seq_lens or scale tensor
+    would otherwise be read or written out of bounds."""
+    if q.dim() != (4 if chunk else 3):
+        raise ValueError(f"q must be [B, Hq, {'T, ' if chunk else ''}D], "
+                         f"got {tuple(q.shape)}")
+    if k.dim() != 4:
+        raise ValueError(f"k_cache must have 4 dimensions, got {tuple(k.shape)}")
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"v_cache {tuple(v.shape)} must have k_cache's shape "
+                         f"{tuple(k.shape)}")
+    B, D = q.shape[0], q.shape[-1]
+    if k.shape[3] != D:
+        raise ValueError(f"k_cache head_dim {k.shape[3]} != q head_dim {D}")
+    if not paged and k.shape[0] != B:
+        raise ValueError(f"k_cache batch {k.shape[0]} != q batch {B}")
+    if tuple(seq_lens.shape) != (B,):
+        raise ValueError(f"seq_lens must be [{B}], got {tuple(seq_lens.shape)}")
+    if tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype:
+        raise ValueError(f"out must match q ({tuple(q.shape)}, {q.dtype}), got "
+                         f"({tuple(out.shape)}, {out.dtype})")
+    for name, sc in (scales or ()):
+        if tuple(sc.shape) != (B, k.shape[1]):
+            raise ValueError(f"{name} must be [{B}, {k.shape[1]}], got "
+                             f"{tuple(sc.shape)}")
+    tensors = [q, k, v, seq_lens, out] + [sc for _, sc in (scales or ())]
+    if any(t.device != q.device for t in tensors):
+        raise ValueError("all tensors must be on the same device")
+
+
 def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out=None,
                stream=None):
     """One GQA decode step; returns ``out`` [B, Hq, D].
@@ -171,6 +211,7 @@ def gqa_decode(q, k_cache, v_cache, seq_lens, scale: float, out=None,
     if out is None:
         out = torch.empty_like(q)
     _check_dev("out", out)
+    _check_layout(q, k_cache, v_cache, seq_lens, out)
     st = lib().gqa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                           seq_lens.data_ptr(), float(scale), out.data_ptr(),
                           B, Hq, Hkv, Smax, D, _dtype_code(q),
@@ -192,11 +233,14 @@ def gqa_decode_chunk(q, k_cache, v_cache, seq_lens, scale: float, out=None,
         raise TypeError("q, k_cache and v_cache must share a dtype")
     if seq_lens.dtype != torch.int32:
         raise TypeError("seq_lens must be int32")
+    if q.dim() != 4:
+        raise ValueError(f"q must be [B, Hq, T, D], got {tuple(q.shape)}")
     B, Hq, T, D = q.shape
     _, Hkv, Smax, _ = k_cache.shape
     if out is None:
         out = torch.empty_like(q)
     _check_dev("out", out)
+    _check_layout(q, k_cache, v_cache, seq_lens, out, chunk=True)
     st = lib().gqa_decode_chunk(q.data_ptr(), k_cache.data_ptr(),
                                 v_cache.data_ptr(), seq_lens.data_ptr(),
                                 float(scale), out.data_ptr(), B, Hq, Hkv, T,
@@ -234,7 +278,20 @@ def gqa_append_kv(k_new, v_new, k_cache, v_cache, seq_lens, k_scale=None,
             if t.dtype != torch.float32:
                 raise TypeError(f"{n} must be float32")
         ks, vs = k_scale.data_ptr(), v_scale.data_ptr()
+    if k_cache.dim() != 4 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must both be [B, Hkv, Smax, D]")
     B, Hkv, Smax, D = k_cache.shape
+    for n, t in (("k_new", k_new), ("v_new", v_new)):
+        if tuple(t.shape) != (B, Hkv, D):
+            raise ValueError(f"{n} must be [{B}, {Hkv}, {D}], got "
+                             f"{tuple(t.shape)}")
+    if tuple(seq_lens.shape) != (B,):
+        raise ValueError(f"seq_lens must be [{B}], got {tuple(seq_lens.shape)}")
+    if cache_code in (GQA_E4M3, GQA_E5M2):
+        for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if tuple(t.shape) != (B, Hkv):
+                raise ValueError(f"{n} must be [{B}, {Hkv}], got "
+                                 f"{tuple(t.shape)}")
     st = lib().gqa_append_kv(k_new.data_ptr(), v_new.data_ptr(),
                              k_cache.data_ptr(), v_cache.data_ptr(), ks, vs,
                              seq_lens.data_ptr(), B, Hkv, Smax, D, in_code,
@@ -264,10 +321,16 @@ def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens,
         raise ValueError("k_pages and v_pages must have the same shape")
     B, Hq, D = q.shape
     num_pages, Hkv, page_size, _ = k_pages.shape
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table must be [{B}, max_pages], got "
+                         f"{tuple(block_table.shape)}")
     max_pages = block_table.shape[1]
     if out is None:
         out = torch.empty_like(q)
     _check_dev("out", out)
+    _check_layout(q, k_pages, v_pages, seq_lens, out, paged=True)
+    if block_table.device != q.device:
+        raise ValueError("all tensors must be on the same device")
     st = lib().gqa_decode_paged(q.data_ptr(), k_pages.data_ptr(),
                                 v_pages.data_ptr(), block_table.data_ptr(),
                                 seq_lens.data_ptr(), float(scale),
@@ -299,6 +362,7 @@ def gqa_decode_static(q, k_cache, v_cache, seq_lens, scale: float, out=None,
     if out is None:
         out = torch.empty_like(q)
     _check_dev("out", out)
+    _check_layout(q, k_cache, v_cache, seq_lens, out)
     st = lib().gqa_decode_static(q.data_ptr(), k_cache.data_ptr(),
                                  v_cache.data_ptr(), seq_lens.data_ptr(),
                                  float(scale), out.data_ptr(), B, Hq, Hkv,
@@ -334,6 +398,8 @@ def gqa_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens,
     if out is None:
         out = torch.empty_like(q)
     _check_dev("out", out)
+    _check_layout(q, k_cache, v_cache, seq_lens, out,
+                  scales=(("k_scale", k_scale), ("v_scale", v_scale)))
     st = lib().gqa_decode_fp8(q.data_ptr(), k_cache.data_ptr(),
                               v_cache.data_ptr(), k_scale.data_ptr(),
                               v_scale.data_ptr(), seq_lens.data_ptr(),

@@ -156,11 +156,12 @@ struct DeviceInfo {
 std::map<int, DeviceInfo> g_dev;
 
 // Scratch per (device, stream), in two allocations:
-//  * ctl  = [error flags (kHeaderBytes) | arrival counters, one per unit].
-//    Zeroed once when allocated; the kernels leave every counter at zero when
-//    they finish, so the region holds zeros between calls and is never
-//    re-initialised.  It is never shared with the partials: a counter must not
-//    land on bytes a previous call used for partial results.
+//  * ctl  = [error flags (kHeaderBytes) | arrival counters, 8 bytes per unit].
+//    Zeroed once when allocated and never re-initialised between calls: each
+//    launch tags its counts with its own generation (DecodeParams::gen), and
+//    a launch that completes leaves every counter at zero, so whatever an
+//    earlier launch left behind is never read as an arrival of this one.  It
+//    is never shared with the partials.
 //  * part = [partial log2-sum-exp | partial O], fully written before it is
 //    read within one call; no initial value needed.
 struct Scratch {
@@ -168,10 +169,18 @@ struct Scratch {
   size_t ctl_units = 0;  // counter capacity
   void* part = nullptr;
   size_t part_bytes = 0;
+  uint32_t gen = 0;      // generation of the last launch on this stream
 };
+
+constexpr size_t kCounterBytes = 8;
+
+// Next launch generation after `g` (0 is never used: zeroed counters carry
+// no generation).
+uint32_t next_gen(uint32_t g) { return g + 1u == 0u ? 1u : g + 1u; }
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 
 int g_num_ctas_override = 0;
+uint64_t g_wait_ns = kWaitLimitNs;
 thread_local int t_last_launches = 0;
 
 constexpr size_t kHeaderBytes = 256;  // error word(s)
@@ -210,12 +219,13 @@ cudaError_t scratch_for(int dev, cudaStream_t stream, size_t units,
   if (s.ctl_units < units || !s.ctl) {
     const size_t cap = align_up(units + units / 4 + 1024, 1024);
     void* ctl = nullptr;
-    cudaError_t e = cudaMallocAsync(&ctl, kHeaderBytes + cap * 4, stream);
+    cudaError_t e =
+        cudaMallocAsync(&ctl, kHeaderBytes + cap * kCounterBytes, stream);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(ctl, 0, kHeaderBytes + cap * 4, stream);
+    e = cudaMemsetAsync(ctl, 0, kHeaderBytes + cap * kCounterBytes, stream);
     if (e != cudaSuccess) return e;
     if (s.ctl) {
-      // carry the error flags over; the old counters are all zero
+      // carry the error flags over to the new, zeroed region
       e = cudaMemcpyAsync(ctl, s.ctl, sizeof(uint32_t),
                           cudaMemcpyDeviceToDevice, stream);
       if (e != cudaSuccess) return e;
@@ -351,7 +361,10 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.error = reinterpret_cast<uint32_t*>(ctl);
-  p.counters = reinterpret_cast<uint32_t*>(ctl + kHeaderBytes);
+  p.counters = reinterpret_cast<unsigned long long*>(ctl + kHeaderBytes);
+  sc->gen = next_gen(sc->gen);
+  p.gen = sc->gen;
+  p.wait_ns = g_wait_ns;
   p.part_lse = reinterpret_cast<float*>(part);
   p.part_o = reinterpret_cast<float*>(part + lse_bytes);
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -410,6 +423,7 @@ namespace {
 // that device current).  The host-side name of the array is only a stand-in:
 // a kernel must be given this address instead.
 std::map<int, void*> g_static_addr;
+std::map<int, uint32_t> g_static_gen;  // last launch generation per device
 
 cudaError_t static_scratch_addr(int dev, void** out) {
   auto it = g_static_addr.find(dev);
@@ -461,7 +475,8 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
                        : static_cast<int>(max_tiles < wave ? max_tiles : wave);
 
   const size_t slots = static_cast<size_t>(grid) + static_cast<size_t>(units);
-  const size_t cnt_bytes = align_up(static_cast<size_t>(units) * 4, 256);
+  const size_t cnt_bytes =
+      align_up(static_cast<size_t>(units) * kCounterBytes, 256);
   const size_t lse_bytes = align_up(slots * rows_pad * 4, 256);
   const size_t o_bytes = slots * rows_pad * static_cast<size_t>(D) * 4;
   const size_t need = kHeaderBytes + cnt_bytes + lse_bytes + o_bytes;
@@ -482,7 +497,11 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
   p.k_scale = nullptr;
   p.v_scale = nullptr;
   p.error = reinterpret_cast<uint32_t*>(wb);
-  p.counters = reinterpret_cast<uint32_t*>(wb + kHeaderBytes);
+  p.counters = reinterpret_cast<unsigned long long*>(wb + kHeaderBytes);
+  uint32_t& gen = g_static_gen[dev];
+  gen = next_gen(gen);
+  p.gen = gen;
+  p.wait_ns = g_wait_ns;
   p.part_lse = reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes);
   p.part_o =
       reinterpret_cast<float*>(wb + kHeaderBytes + cnt_bytes + lse_bytes);
@@ -588,8 +607,20 @@ gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
     return GQA_ERR_CUDA;
   if (v != 0 && cudaMemset(it->second.ctl, 0, 4) != cudaSuccess)
     return GQA_ERR_CUDA;
+  // After a wait gave up some arrival counters may be left non-zero.  Later
+  // launches ignore them (their generation differs), except replays of one
+  // captured launch, which reuse its generation: clear them.
+  if ((v & gqa::kErrWaitTimeout) &&
+      cudaMemset(static_cast<uint8_t*>(it->second.ctl) + gqa::kHeaderBytes, 0,
+                 it->second.ctl_units * gqa::kCounterBytes) != cudaSuccess)
+    return GQA_ERR_CUDA;
   *flags = v;
   return GQA_OK;
+}
+
+void gqa_set_wait_limit_ns(long long ns) {
+  std::lock_guard<std::mutex> lock(gqa::g_mu);
+  gqa::g_wait_ns = ns < 0 ? gqa::kWaitLimitNs : static_cast<uint64_t>(ns);
 }
 
 void gqa_set_num_ctas(int num_ctas) {

@@ -58,7 +58,9 @@
 //    otherwise each block writes a normalised partial (O, log2-sum-exp) and
 //    bumps a per-unit counter; the block that arrives last merges all
 //    partials of the unit (after its own last unit) and writes the output,
-//    then resets the counter.  No block ever waits on another block.
+//    then resets the counter.  No block ever waits on another block.  The
+//    counters carry the launch's generation, so a count that a launch left
+//    behind (because one of its waits gave up) is never taken for this one's.
 //  * Paged cache (PAGED).  Only the producer changes: each tile's page comes
 //    from the block table and the TMA load addresses (row in page, page x
 //    Hkv + KV head) of the page pool [pages x Hkv][page_size][D].
@@ -97,8 +99,13 @@ static_assert(128 * kRegsSmall + 256 * kRegsBig <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int kMaxUnitRows = 64;  // query heads per unit (4 head blocks)
 constexpr int kPrefetchTiles = 12; // tiles per block warmed in L2 at launch
+// Default time limit of a pipeline wait (DecodeParams::wait_ns); the drain of
+// a block's own bulk copies before it exits always uses kDrainLimitNs.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
+// Retries of the compare-and-swap that counts a block's arrival at a unit
+// (each failure means another block's arrival succeeded, so a few suffice).
+constexpr int kMaxArrivalTries = 1 << 16;
 // Dynamic shared memory per block: the sm_100-family opt-in maximum (227 KB)
 // less 512 bytes left for the kernel's static shared variables.
 constexpr int kSmemBudget = 232448 - 512;
@@ -124,8 +131,12 @@ struct DecodeParams {
   const float* v_scale;     // [B, Hkv] (E4M3 only)
   float* part_o;            // [slots, rows_pad, D]  normalised partial outputs
   float* part_lse;          // [slots, rows_pad]     log2-sum-exp of partials
-  uint32_t* counters;       // [units] arrivals per unit (zero between calls)
+  // [units] arrivals per unit: (launch generation << 32) | blocks arrived;
+  // a value that carries another launch's generation counts as zero
+  unsigned long long* counters;
   uint32_t* error;          // fault flags
+  uint32_t gen;             // this launch's generation (never 0)
+  uint64_t wait_ns;         // time limit of a pipeline wait (0: give up at once)
   // paged cache only: block_table[b * max_pages + i] is the page holding
   // tokens [i * page_size, (i + 1) * page_size) of sequence b
   const int32_t* block_table;
@@ -670,7 +681,32 @@ __device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
                           acc[x], (lt[x] > 0.f ? 1.f / lt[x] : 0.f) * om);
     }
   }
-  if (t == 0) p.counters[u] = 0u;
+  if (t == 0) p.counters[u] = 0ull;
+}
+
+// Counts this block's arrival at unit u (after its partial is stored) and
+// returns how many blocks of this launch arrived before it.  The counter
+// carries the launch generation in its upper half: a value another launch
+// left behind (one whose waits gave up before all its blocks arrived) counts
+// as no arrival, so such a launch cannot shift the tickets of later ones.
+// The swap has acquire-release semantics: the caller's partial stores (and
+// those ordered before it by a barrier) are released, and the last arriver
+// sees every other block's.  Sets kErrWaitTimeout and returns a ticket that
+// matches no arrival count if the swap keeps failing.
+__device__ __forceinline__ uint32_t arrive_unit(const DecodeParams& p, int u) {
+  unsigned long long* c = p.counters + u;
+  const unsigned long long tag = static_cast<unsigned long long>(p.gen) << 32;
+  unsigned long long cur = ptx::ld_relaxed_gpu(c);
+  for (int i = 0; i < kMaxArrivalTries; ++i) {
+    const uint32_t n =
+        (cur >> 32) == p.gen ? static_cast<uint32_t>(cur) : 0u;
+    const unsigned long long seen =
+        ptx::atom_cas_acq_rel_gpu(c, cur, tag | (n + 1u));
+    if (seen == cur) return n;
+    cur = seen;
+  }
+  atomicOr(p.error, kErrWaitTimeout);
+  return 0xffffffffu;
 }
 
 // Warms L2 with this block's first tiles, guessing that every sequence fills
@@ -898,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (PAGED)
           pg = __ldg(p.block_table + static_cast<size_t>(w.b) * p.max_pages +
                      tok / p.page_size);
-        if (!ptx::mbar_wait_bounded(&empty[stage], ph ^ 1u, kWaitLimitNs)) {
+        if (!ptx::mbar_wait_bounded(&empty[stage], ph ^ 1u, p.wait_ns)) {
           atomicOr(p.error, kErrWaitTimeout);
           s_abort = 1;
           break;
@@ -956,9 +992,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // unit is merged by the consumers themselves (descriptor s_dstop).
     uint32_t kph = 0;  // parity of the dump being waited for
     while (true) {
-      if (!ptx::mbar_wait_bounded(dump_full, kph, kWaitLimitNs)) {
-        atomicOr(p.error, kErrWaitTimeout);
-        s_abort = 1;
+      // Every merge thread waits; the give-up decision is taken together
+      // (barrier with an OR of the outcomes), so that all merge warps either
+      // go on to merge_unit's barriers or leave.
+      const bool ok = ptx::mbar_wait_bounded(dump_full, kph, p.wait_ns);
+      if (ptx::named_bar_or(2, kMergeThreads, !ok)) {
+        if (mt == 0) {
+          atomicOr(p.error, kErrWaitTimeout);
+          s_abort = 1;
+        }
         return;
       }
       kph ^= 1u;
@@ -974,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mt == 0) {
         if (!whole && s_npend < 2) {
           const int k = s_npend;
-          s_pend_t[k] = ptx::atom_add_acq_rel_gpu(p.counters + u, 1u);
+          s_pend_t[k] = arrive_unit(p, u);
           s_pend_u[k] = u;
           s_pend_b[k] = bq;
           s_pend_j[k] = j;
@@ -1055,7 +1097,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (par == grp) {
     // ---- wait for the stage (the groups take the tiles in turn) ----
-    if (!aborted && !ptx::mbar_wait_bounded(&full[stage], ph, kWaitLimitNs)) {
+    // the warp decides together (a lane-divergent give-up would leave its
+    // lanes on different paths)
+    if (!aborted &&
+        !__all_sync(0xffffffffu,
+                    ptx::mbar_wait_bounded(&full[stage], ph, p.wait_ns))) {
       atomicOr(p.error, kErrWaitTimeout);
       aborted = true;
       s_abort = 1;  // stops the producer
@@ -1430,7 +1476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ============ unit epilogue: hand the state to the merge warps ========
       // wait until the merge warps have finished with the previous dump
       if (!aborted &&
-          !ptx::mbar_wait_bounded(dump_empty, dph ^ 1u, kWaitLimitNs)) {
+          !__all_sync(0xffffffffu,
+                      ptx::mbar_wait_bounded(dump_empty, dph ^ 1u,
+                                             p.wait_ns))) {
         atomicOr(p.error, kErrWaitTimeout);
         aborted = true;
         s_abort = 1;
@@ -1579,7 +1627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ct == 0) {
       if (!whole && s_npend < 2) {
         const int k = s_npend;
-        s_pend_t[k] = ptx::atom_add_acq_rel_gpu(p.counters + u, 1u);
+        s_pend_t[k] = arrive_unit(p, u);
         s_pend_u[k] = u;
         s_pend_b[k] = s_db;
         s_pend_j[k] = s_dj;

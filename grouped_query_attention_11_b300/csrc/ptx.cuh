@@ -86,10 +86,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar,
 // wait in these kernels can spin forever.  A waiting warp sleeps in its
 // try_wait instead of polling, leaving the issue slots of its SM
 // sub-partition to the warps that compute.
+//
+// limit_ns == 0 gives up at once when the phase is not already complete
+// (a test setting: it makes a wait run out without withholding any work).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar,
                                                   uint32_t parity,
                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (limit_ns == 0) return false;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
@@ -250,29 +254,27 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Global atomic add with release semantics at GPU scope (orders the calling
-// thread's prior writes, and those ordered before it by a CTA barrier,
-// before the add).
-__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* addr,
-                                                         uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;"
-               : "=r"(old)
-               : "l"(addr), "r"(v)
+// 64-bit compare-and-swap with acquire-release semantics at GPU scope;
+// returns the value found at addr (== expected when the swap happened).
+__device__ __forceinline__ unsigned long long atom_cas_acq_rel_gpu(
+    unsigned long long* addr, unsigned long long expected,
+    unsigned long long desired) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old)
+               : "l"(addr), "l"(expected), "l"(desired)
                : "memory");
   return old;
 }
 
-// The same with acquire-release semantics: additionally, what other threads
-// released before their adds is visible to the caller afterwards.
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* addr,
-                                                         uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-               : "=r"(old)
-               : "l"(addr), "r"(v)
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(
+    const unsigned long long* addr) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];"
+               : "=l"(v)
+               : "l"(addr)
                : "memory");
-  return old;
+  return v;
 }
 
 // Warpgroup register reallocation: every warp of a warpgroup executes the
@@ -290,6 +292,21 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets true when any of them passed true.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 }  // namespace ptx

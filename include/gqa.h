@@ -259,12 +259,31 @@ const char* gqa_status_string(gqa_status status);
 /*
  * gqa_device_errors — synchronises `stream`, then returns (and clears) the
  * fault flags the kernels raised on it since the last query: 0 when none.
- * Bit 0: a pipeline wait gave up after its time limit (the affected outputs
- * are unspecified).  Bit 1: a paged call met a block-table entry outside
- * [0, num_pages).  Bit 2: an append found a sequence's cache full.
+ * Bit 0: a pipeline wait gave up after its time limit (the outputs of that
+ * call are unspecified; the kernel still finished and left the GPU usable).
+ * Bit 1: a paged call met a block-table entry outside [0, num_pages).
+ * Bit 2: an append found a sequence's cache full.
  * Returns GQA_ERR_CUDA if the synchronisation fails.
+ *
+ * Recovery after bit 0.  A call whose wait gave up may leave some of the
+ * stream's split-combine arrival counters non-zero.  Later calls are not
+ * affected: every call tags its counts with a generation of its own and
+ * ignores counts another call left.  The one exception is a call captured in
+ * a CUDA graph, whose replays share one generation; when this function finds
+ * bit 0 set it therefore also clears the stream's counters, after which
+ * replays are correct again.
  */
 gqa_status gqa_device_errors(void* stream, uint32_t* flags);
+
+/*
+ * gqa_set_wait_limit_ns — test hook: the time limit of every pipeline wait in
+ * the decode kernels launched afterwards (process-wide; host only).  A wait
+ * that runs out sets bit 0 of gqa_device_errors, and the kernel stops waiting
+ * and finishes.  ns = 0 gives up at the first wait that is not already
+ * complete (so a test can make a wait run out without withholding any work);
+ * ns < 0 restores the default of 2 seconds.
+ */
+void gqa_set_wait_limit_ns(long long ns);
 
 /*
  * gqa_set_num_ctas — test and tuning hook: fixes the number of persistent

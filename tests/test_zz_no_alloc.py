@@ -81,6 +81,46 @@ def test_static_scratch_two_calls_in_a_row_same_inputs():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
+def _pool_used_bytes(device: int) -> int:
+    """Bytes in use from the device's default memory pool, the pool the
+    library's stream-ordered scratch allocations come from."""
+    from cuda.bindings import runtime as rt
+    err, pool = rt.cudaDeviceGetDefaultMemPool(device)
+    assert err == rt.cudaError_t.cudaSuccess, err
+    err, v = rt.cudaMemPoolGetAttribute(
+        pool, rt.cudaMemPoolAttr.cudaMemPoolAttrUsedMemCurrent)
+    assert err == rt.cudaError_t.cudaSuccess, err
+    return int(v)
+
+
+def test_static_entry_point_allocates_nothing():
+    """On a stream the allocating entry point has never seen, two calls of
+    gqa_decode_static leave the device pool's usage unchanged (no per-stream
+    scratch is created), and still match gqa_decode.  Control: the first
+    gqa_decode call on a new stream does take its scratch from that pool, so
+    the measurement would see an allocation."""
+    w = Workload("static_d", 3, 64, 8, 128, 1200, "bf16",
+                 lens=("list", 1200, 5, 640), seed=74)
+    d = to_device(make_inputs(w, pad="nan"))
+    ref = gq.gqa_decode(d["q"], d["k"], d["v"], d["seq_lens"], d["scale"])
+    out = torch.empty_like(d["q"])
+    torch.cuda.synchronize()
+    dev = torch.cuda.current_device()
+    fresh = torch.cuda.Stream()
+    before = _pool_used_bytes(dev)
+    for _ in range(2):
+        assert _call_static(d, out, fresh) == gq.GQA_OK
+    fresh.synchronize()
+    assert _pool_used_bytes(dev) == before
+    _check_pair(out, ref)
+
+    other = torch.cuda.Stream()
+    gq.gqa_decode(d["q"], d["k"], d["v"], d["seq_lens"], d["scale"],
+                  out=out, stream=other)
+    other.synchronize()
+    assert _pool_used_bytes(dev) > before
+
+
 def test_static_scratch_refuses_oversized_request():
     # B=32, Hq=Hkv=64, D=128 needs about 18 MB of scratch: refused with
     # GQA_ERR_UNSUPPORTED before anything is enqueued (the pointers are
