@@ -3,21 +3,43 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-cpu-baseline]
+                    [--no-per-config] [--op decode|append]
 
 One step = one gqa_decode call over the whole batch of the workload (default:
 the Llama-2/3-70B-shaped long-context decode, B=8, Hq=64, Hkv=8, D=128,
 seq_len=8192, bf16).  Inputs are synthetic, seeded, and resident in HBM when
-the timed region starts; they exceed the 126 MB L2 (268 MB for the default
-workload) and the kernel loads K/V with an L2 evict-first hint, so nothing is
-flushed between steps.  Each step is bracketed by CUDA events recorded on the
-launching stream; the timed region is bracketed by a barrier and
-torch.cuda.synchronize() on both sides.
+the timed region starts.
 
-Printed (rank 0, one JSON line): the metric (us/step, lower is better), KV
-GB/s and the HBM roofline fraction, an end-to-end figure through the public
-API with host buffers (pinned H2D of the step's inputs + decode + D2H of the
-output), SM clocks sampled during the timed region, and the fp64 CPU oracle
-timed on a bounded sample of the same workload (``cpu_baseline``).
+Protocol of the headline line:
+
+1. the nvidia-smi clock sampler starts and settles (1 s, the GPU idle);
+2. W warm-up steps, then back-to-back steps until SETTLE_S seconds have passed
+   since the warm-up began ("settle"): the first ~1 ms of work after an idle
+   GPU runs up to 25 % slower, with the SM and memory clocks already at their
+   maximum, so a short timed region that follows an idle gap measures that
+   ramp rather than the kernel;
+3. barrier + synchronize, then EXACTLY K steps back to back between two CUDA
+   events on the launching stream (one pre-marshalled C-ABI call per step),
+   barrier + synchronize.  The inputs (268 MB) exceed the 126 MB L2 and K/V are
+   loaded evict-first, so nothing is flushed between steps.
+
+After the timed region (not part of ``value``): the same K-step region
+repeated (median, p10, p90) and the per-launch time of steps that each start
+with a flushed L2 (a 256 MB buffer written before every step; median, p10,
+p90 of 200).
+
+``per_config`` (N=1): every other named workload measured in the same process
+by the same steps, with inputs drawn on the device.  Workloads whose bytes
+per step exceed twice the L2 are timed back to back; smaller ones (tiny, the
+8B shape, MQA) with L2 flushed before every step, so that their figure is an
+HBM figure.  Each entry carries us/step, KV GB/s, the roofline fraction, the
+profiled DRAM traffic (when current) and the CPU oracle on a bounded sample.
+
+The headline line also carries an end-to-end figure through the public API
+with host buffers (pinned H2D of the step's inputs + decode + D2H of the
+output), SM clocks sampled from the warm-up to the end of the timed region,
+and the fp64 CPU oracle timed on a bounded sample of the same workload
+(``cpu_baseline``).
 
 ``--impl reference`` times only that oracle (the reference arm): each step is
 a bounded sample of the workload, extrapolated to the metric's unit.
@@ -47,7 +69,8 @@ SPEC_HBM_GBS = 8000.0
 L2_BYTES = 126 * 1024 * 1024
 
 
-KERNEL_SOURCES = ("gqa_decode_kernel.cuh", "ptx.cuh", "gqa_api.cu")
+KERNEL_SOURCES = ("gqa_decode_kernel.cuh", "gqa_decode_umma.cuh", "ptx.cuh",
+                  "gqa_api.cu", "gqa_umma.cu")
 GRAPH_STEPS = 100  # steps per captured CUDA graph (--graph, --op append)
 
 
@@ -135,10 +158,11 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 200):
+    def __init__(self, gpu_index: int, period_ms: int = 100):
         self.proc = None
         self.rows = []
         self.gpu_index = gpu_index
+        self.t_mark = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}",
@@ -147,6 +171,11 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+
+    def mark(self):
+        """Only samples taken from now on count in summary()."""
+        import datetime
+        self.t_mark = datetime.datetime.now()
 
     def stop(self):
         if self.proc is None:
@@ -162,58 +191,207 @@ class ClockSampler:
             if len(parts) >= 10:
                 self.rows.append(parts)
 
+    def _window(self):
+        if self.t_mark is None:
+            return self.rows
+        import datetime
+        kept = []
+        for r in self.rows:
+            try:
+                t = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            if t >= self.t_mark:
+                kept.append(r)
+        return kept or self.rows[-1:]
+
     def summary(self):
-        if not self.rows:
+        rows = self._window()
+        if not rows:
             return None
-        sm = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in self.rows if r[3].replace(".", "").isdigit()]
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         reasons = set()
-        for r in self.rows:
+        for r in rows:
             for name, val in zip(names, r[6:10]):
                 if val.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.rows)}
+                "reasons": sorted(reasons), "samples": len(rows)}
 
 
 # ------------------------------------------------------------ CPU baseline
 
+def _host_sequence(inp: dict, b: int, pool_host: dict) -> dict:
+    """Sequence b of a workload's inputs as host tensors (the inputs may be
+    on the device; a paged cache's page pool is copied to the host once)."""
+    out = {"scale": inp["scale"]}
+    sl = slice(b, b + 1)
+    for key in ("q", "seq_lens", "k_scale", "v_scale", "block_table"):
+        v = inp.get(key)
+        out[key] = v[sl].cpu() if v is not None else None
+    if inp.get("block_table") is not None:
+        for key in ("k", "v"):
+            if key not in pool_host:
+                pool_host[key] = inp[key].cpu()
+            out[key] = pool_host[key]
+    else:
+        for key in ("k", "v"):
+            out[key] = inp[key][sl].cpu()
+    return out
+
+
 def cpu_baseline(w, inp, budget_s: float = 10.0):
     """fp64 oracle on the host cores: whole sequences, one at a time, until
-    ``budget_s`` has passed; extrapolated to one full step (us/step)."""
-    import numpy as np
+    ``budget_s`` of oracle time has passed; extrapolated to one full step
+    (us/step).  Only the oracle calls are timed (not the copies of each
+    sequence's inputs to the host)."""
     import oracle
-    import torch
     oracle.build()
     threads = oracle.max_threads()
-    lens = inp["seq_lens"]
-    done_tokens = 0
+    lens = inp["seq_lens"].cpu()
     total_tokens = int(lens.sum())
-    t0 = time.perf_counter()
-    n_seq = 0
-    order = list(range(w.B))
-    for b in order:
-        sl = slice(b, b + 1)
-        ks = inp["k_scale"][sl] if inp["k_scale"] is not None else None
-        vs = inp["v_scale"][sl] if inp["v_scale"] is not None else None
-        oracle.gqa_decode(inp["q"][sl], inp["k"][sl], inp["v"][sl], lens[sl],
-                          inp["scale"], k_scale=ks, v_scale=vs,
-                          nthreads=threads)
+    done_tokens, n_seq, el = 0, 0, 0.0
+    pool_host = {}
+    for b in range(w.B):
+        h = _host_sequence(inp, b, pool_host)
+        t0 = time.perf_counter()
+        if h["q"].dim() == 4:
+            oracle.gqa_decode_chunk(h["q"], h["k"], h["v"], h["seq_lens"],
+                                    h["scale"], nthreads=threads)
+        elif h["block_table"] is not None:
+            oracle.gqa_decode_paged(h["q"], h["k"], h["v"], h["block_table"],
+                                    h["seq_lens"], h["scale"],
+                                    nthreads=threads)
+        else:
+            oracle.gqa_decode(h["q"], h["k"], h["v"], h["seq_lens"],
+                              h["scale"], k_scale=h["k_scale"],
+                              v_scale=h["v_scale"], nthreads=threads)
+        el += time.perf_counter() - t0
         done_tokens += int(lens[b])
         n_seq += 1
-        if time.perf_counter() - t0 >= budget_s:
+        if el >= budget_s:
             break
-    el = time.perf_counter() - t0
     frac = done_tokens / total_tokens if total_tokens else 1.0
     us_per_step = el / frac * 1e6 if frac > 0 else el * 1e6
     return {"value": us_per_step, "unit": "us/step", "cores": threads,
             "kind": "oracle",
             "sample": (f"{n_seq} of {w.B} sequences ({done_tokens} of "
-                       f"{total_tokens} tokens, all {w.Hq} query heads), fp64 "
-                       f"C oracle, {el:.2f} s wall, extrapolated by tokens")}
+                       f"{total_tokens} tokens, all {w.Hq} query heads"
+                       f"{f', {w.T} tokens each' if w.T > 1 else ''}), fp64 "
+                       f"C oracle, {el:.2f} s, extrapolated by tokens")}
+
+
+# ------------------------------------------------------------------ timing
+
+SETTLE_S = 0.25        # back-to-back steps after the warm-up, seconds
+COLD_STEPS = 200       # flushed-L2 launches timed one by one
+REPEATS = 30           # K-step regions repeated after the timed one
+
+
+def _pct(xs, q):
+    xs = sorted(xs)
+    if not xs:
+        return None
+    k = (len(xs) - 1) * q
+    lo = int(k)
+    hi = min(lo + 1, len(xs) - 1)
+    return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+
+
+def _dist(xs):
+    return {"median_us": _pct(xs, 0.5), "p10_us": _pct(xs, 0.1),
+            "p90_us": _pct(xs, 0.9), "n": len(xs)}
+
+
+def time_region(step, K: int, stream) -> float:
+    """us per step of K back-to-back steps between two events on the
+    launching stream (synchronised on both sides)."""
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / K
+
+
+def settle(step, seconds: float) -> int:
+    """Back-to-back steps until `seconds` of host time have passed (the
+    launch queue keeps the GPU busy throughout); returns their number."""
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(20):
+            step()
+        n += 20
+    return n
+
+
+def cold_launches(step, n: int, stream, flush) -> list:
+    """Per-launch us of n steps, each after writing a buffer twice the size
+    of L2 (so the step finds none of its inputs in L2 and no earlier decode
+    launch to overlap with)."""
+    import torch
+    evs = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in evs]
+
+
+def measure_config(name, w, dev, stream, flush, warmup, K, peak, peak_kind,
+                   cpu_budget):
+    """One per_config entry: the workload's inputs drawn on the device, warm-up
+    and settle as for the headline, then either K-step back-to-back regions
+    (bytes per step > 2 x L2) or flushed-L2 launches one by one."""
+    import torch
+    import grouped_query_attention_11_b300 as gq
+    from grouped_query_attention_11_b300.workloads import make_inputs
+    inp = make_inputs(w, pad="zero", device=dev)
+    inp.pop("k_contig", None)
+    inp.pop("v_contig", None)
+    out = torch.empty_like(inp["q"])
+    step = gq.BoundDecode(inp, out, stream)
+    algo = w.algorithmic_bytes(inp["seq_lens"].cpu())
+    for _ in range(warmup):
+        step()
+    settle(step, 0.1)
+    torch.cuda.synchronize()
+    assert gq.gqa_device_errors(stream) == 0
+    b2b = [time_region(step, K, stream) for _ in range(5)]
+    cold = cold_launches(step, 50, stream, flush)
+    big = algo > 2 * L2_BYTES
+    us = _pct(b2b, 0.5) if big else _pct(cold, 0.5)
+    assert gq.gqa_device_errors(stream) == 0
+    achieved = algo / (us * 1e-6) / 1e9
+    entry = {
+        "workload": name, "us_per_step": us,
+        "l2": ("back to back: inputs larger than 2 x L2, median of 5 "
+               f"regions of {K} steps") if big else
+              "L2 flushed before every step: median of 50 launches",
+        "kv_gbs": achieved, "frac": achieved / peak, "peak": peak,
+        "peak_kind": peak_kind, "algorithmic_bytes_per_step": algo,
+        "traffic": profiled_traffic(name),
+        "back_to_back": _dist(b2b), "cold_l2": _dist(cold),
+        "launches_per_step": gq.gqa_last_launch_count(),
+    }
+    if cpu_budget > 0:
+        entry["cpu_baseline"] = cpu_baseline(w, inp, budget_s=cpu_budget)
+    del inp, out, step
+    torch.cuda.empty_cache()
+    return entry
 
 
 # ------------------------------------------------------------------ runner
@@ -354,6 +532,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload measurements (headline only)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--op", default="decode", choices=["decode", "append"],
                     help="decode: the decode step (default); append: the "
@@ -418,6 +598,7 @@ def main(argv=None):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
     gq.lib()
+    gq.gqa_set_num_ctas(0)
 
     inp = make_inputs(w, pad="zero", seed=w.seed + rank)
     # a paged workload also carries its contiguous copy (for checks): not an
@@ -428,31 +609,30 @@ def main(argv=None):
          for k, v in inp.items()}
     out = torch.empty_like(d["q"])
     stream = torch.cuda.current_stream()
-
     step = gq.BoundDecode(d, out, stream)
-
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    assert gq.gqa_device_errors(stream) == 0
-
     algo_bytes = w.algorithmic_bytes(inp["seq_lens"])
     K = a.steps
-    # K steps back to back between one pair of events on the launching
-    # stream; the host only enqueues (one C-ABI call per step), so the device
-    # time per step is not inflated by Python overhead.
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
 
+    # clock sampler first, while the GPU is idle; then warm-up and settle, so
+    # that the timed steps follow back-to-back work directly
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(1.0 if sampler and sampler.proc else 0)
+    if sampler:
+        sampler.mark()
+    for _ in range(warmup):
+        step()
+    n_settle = settle(step, SETTLE_S)
+
+    # ---- the timed region: exactly K steps ----
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches = 0
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.perf_counter()
     ev0.record(stream)
-    for i in range(K):
+    for _ in range(K):
         step()
         launches += gq.gqa_last_launch_count()
     ev1.record(stream)
@@ -463,13 +643,17 @@ def main(argv=None):
     if sampler:
         sampler.stop()
     assert gq.gqa_device_errors(stream) == 0
-
     us = ev0.elapsed_time(ev1) * 1e3 / K
     # replicas: every rank ran K steps; the job's time is the slowest rank's
     job_us = job_us_per_step(us, ws, dev)
 
+    # ---- distributions (after the timed region; not part of value) ----
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    repeats = [time_region(step, K, stream) for _ in range(REPEATS)]
+    cold = cold_launches(step, COLD_STEPS, stream, flush)
+    assert gq.gqa_device_errors(stream) == 0
+
     # ---- end to end through the public API, host buffers ----
-    e2e = None
     ek = max(1, a.e2e_steps)
     host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v)
             for k, v in inp.items()}
@@ -510,9 +694,29 @@ def main(argv=None):
     achieved = algo_bytes / (us * 1e-6) / 1e9
     traffic = profiled_traffic(name)
     clocks = sampler.summary() if sampler else None
+    if clocks is not None:
+        clocks["window"] = "warm-up, settle and timed region"
     cpu = None
     if not a.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, inp, budget_s=10.0)
+
+    per_config = None
+    if ws == 1 and not a.no_per_config:
+        del d, step
+        torch.cuda.empty_cache()
+        per_config = {}
+        pc_sampler = ClockSampler(torch.cuda.current_device())
+        time.sleep(1.0 if pc_sampler.proc else 0)
+        pc_sampler.mark()
+        for cname, cw in WORKLOADS.items():
+            if cname == name:
+                continue
+            per_config[cname] = measure_config(
+                cname, cw, dev, stream, flush, warmup, max(K, 20), peak,
+                peak_kind, 0.0 if a.no_cpu_baseline else 2.0)
+        pc_sampler.stop()
+        per_config["clocks"] = pc_sampler.summary()
+
     line = {
         "metric": METRIC, "value": job_us, "unit": "us/step",
         "n_gpus": ws, "steps": K, "warmup": warmup,
@@ -520,6 +724,8 @@ def main(argv=None):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if
         w.kv == "same" else f"{w.kv} KV / {w.dtype} q,out", "data": "synthetic",
         "config": cfg,
+        "settle": {"steps": n_settle, "seconds": SETTLE_S,
+                   "note": "untimed back-to-back steps after the warm-up"},
         "kv_gbs": achieved * ws, "hbm_frac_of_" + peak_kind: achieved / peak,
         "hbm_frac_of_spec_8tbs": achieved / SPEC_HBM_GBS,
         "wall_s_timed_region": t_wall,
@@ -527,8 +733,11 @@ def main(argv=None):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": traffic},
+        "repeats": dict(_dist(repeats), steps_per_region=K),
+        "cold_l2": _dist(cold),
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:

@@ -21,7 +21,8 @@ its names:
   any device allocation;
 * :func:`gqa_kv_bytes_per_token`, :func:`gqa_status_string`,
   :func:`gqa_device_errors`, :func:`gqa_set_num_ctas`,
-  :func:`gqa_set_wait_limit_ns`, :func:`gqa_last_launch_count`.
+  :func:`gqa_set_wait_limit_ns`, :func:`gqa_set_kernel_path`,
+  :func:`gqa_last_launch_count`.
 """
 from __future__ import annotations
 
@@ -57,6 +58,7 @@ SIGNATURES = {
     "gqa_device_errors": (_I32, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_set_num_ctas": (None, [_I32]),
     "gqa_set_wait_limit_ns": (None, [ctypes.c_longlong]),
+    "gqa_set_kernel_path": (None, [_I32]),
     "gqa_last_launch_count": (_I32, []),
 }
 
@@ -98,6 +100,12 @@ def gqa_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
 
 def gqa_set_num_ctas(n: int) -> None:
     lib().gqa_set_num_ctas(int(n))
+
+
+def gqa_set_kernel_path(path: int) -> None:
+    """Test / tuning hook: 0 automatic, 1 warp-level mma kernel only, 2
+    tensor-core kernel wherever it applies."""
+    lib().gqa_set_kernel_path(int(path))
 
 
 def gqa_set_wait_limit_ns(ns: int) -> None:

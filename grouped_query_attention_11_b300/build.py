@@ -2,8 +2,9 @@
 
     python -m grouped_query_attention_11_b300.build [--verbose-ptxas]
 
-The library is one translation unit (csrc/gqa_api.cu, which includes the
-kernels) linked against the static CUDA runtime, so it loads on a machine
+The library is two translation units (csrc/gqa_api.cu: the C ABI with the
+warp-level kernels; csrc/gqa_umma.cu: the tensor-core kernel), compiled in
+parallel and linked against the static CUDA runtime, so it loads on a machine
 without a GPU driver; the driver is only needed when a compute call runs.
 """
 from __future__ import annotations
@@ -18,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgqa_b300.so")
-SOURCES = [os.path.join(CSRC, "gqa_api.cu")]
+SOURCES = [os.path.join(CSRC, "gqa_api.cu"), os.path.join(CSRC, "gqa_umma.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
                   if f.endswith((".cuh", ".h"))] + [
     os.path.join(INCLUDE, "gqa.h")]
@@ -42,16 +43,32 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, ptxas_verbose: bool = False) -> str:
+    """Compiles each translation unit (in parallel) and links the library."""
     if not force and up_to_date():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC", "-cudart", "static",
-           "-I", INCLUDE, "-I", CSRC, "-o", tmp, *SOURCES]
-    if ptxas_verbose:
-        cmd[1:1] = ["-Xptxas", "-v"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(CSRC, os.path.basename(src) + tag + ".o")
+        cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-c",
+               "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, "-o", obj,
+               src]
+        if ptxas_verbose:
+            cmd[1:1] = ["-Xptxas", "-v"]
+        objs.append(obj)
+        procs.append((cmd, subprocess.Popen(cmd)))
+    try:
+        for cmd, proc in procs:
+            if proc.wait() != 0:
+                raise subprocess.CalledProcessError(proc.returncode, cmd)
+        tmp = LIB + tag
+        subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o",
+                        tmp, *objs], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB
 
 

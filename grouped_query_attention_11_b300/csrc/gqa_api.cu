@@ -1,6 +1,7 @@
 // gqa_api.cu — host side of libgqa_b300.so: the C ABI declared in
 // include/gqa.h (argument checks, TMA descriptors, per-stream scratch,
-// kernel selection and launch).  All GPU work is in gqa_decode_kernel.cuh.
+// kernel selection and launch).  All GPU work is in gqa_decode_kernel.cuh
+// (warp-level mma kernel) and gqa_decode_umma.cuh (tensor-core kernel).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -15,6 +16,7 @@
 #include "gqa.h"
 #include "gqa_append_kernel.cuh"
 #include "gqa_decode_kernel.cuh"
+#include "gqa_umma.h"
 
 namespace gqa {
 namespace {
@@ -61,15 +63,35 @@ bool make_cache_map(CUtensorMap* map, const void* base, int elem_bytes,
   return r == CUDA_SUCCESS;
 }
 
-// Encoded descriptors of recently used caches: a descriptor only records the
-// base address, shape and strides, so it stays valid for any later call on
-// the same (pointer, shape).  Bounded; cleared when full.  Guarded by g_mu.
+// Rank-2 view [rows][D] of the 16-bit queries [B, Hq, T, D] for the
+// tensor-core kernel: box = 64 rows x 64 elements (128-byte rows, 128-byte
+// swizzle), the K-major operand layout of its first product.
+bool make_q_map(CUtensorMap* map, const void* base, long long rows, int D) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kUmmaCols)};
+  cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(
+      map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims,
+      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Encoded descriptors of recently used caches and queries: a descriptor only
+// records the base address, shape and strides, so it stays valid for any
+// later call on the same (pointer, shape).  Bounded; cleared when full.
+// Guarded by g_mu.  kind 0: a cache view, 1: a query view.
 struct MapKey {
   const void* base;
-  int elem_bytes, B, Hkv, Smax, D;
+  int kind, elem_bytes, B, Hkv, Smax, D;
   bool operator<(const MapKey& o) const {
-    return std::tie(base, elem_bytes, B, Hkv, Smax, D) <
-           std::tie(o.base, o.elem_bytes, o.B, o.Hkv, o.Smax, o.D);
+    return std::tie(base, kind, elem_bytes, B, Hkv, Smax, D) <
+           std::tie(o.base, o.kind, o.elem_bytes, o.B, o.Hkv, o.Smax, o.D);
   }
 };
 std::map<MapKey, CUtensorMap> g_maps;
@@ -77,13 +99,26 @@ constexpr size_t kMaxCachedMaps = 256;
 
 bool cached_cache_map(CUtensorMap* map, const void* base, int elem_bytes,
                       int B, int Hkv, int Smax, int D) {
-  const MapKey key{base, elem_bytes, B, Hkv, Smax, D};
+  const MapKey key{base, 0, elem_bytes, B, Hkv, Smax, D};
   auto it = g_maps.find(key);
   if (it != g_maps.end()) {
     *map = it->second;
     return true;
   }
   if (!make_cache_map(map, base, elem_bytes, B, Hkv, Smax, D)) return false;
+  if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+  g_maps.emplace(key, *map);
+  return true;
+}
+
+bool cached_q_map(CUtensorMap* map, const void* base, int rows, int D) {
+  const MapKey key{base, 1, 2, rows, 0, 0, D};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *map = it->second;
+    return true;
+  }
+  if (!make_q_map(map, base, rows, D)) return false;
   if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
   g_maps.emplace(key, *map);
   return true;
@@ -151,7 +186,7 @@ std::mutex g_mu;
 
 struct DeviceInfo {
   int sms = 0;
-  std::map<KernelFn, int> blocks_per_sm;  // configured variants
+  std::map<const void*, int> blocks_per_sm;  // configured kernels
 };
 std::map<int, DeviceInfo> g_dev;
 
@@ -181,34 +216,46 @@ std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 
 int g_num_ctas_override = 0;
 uint64_t g_wait_ns = kWaitLimitNs;
+// Kernel choice: 0 automatic (the tensor-core kernel for units of more than
+// 16 query rows with a 16-bit cache, head_dim 128, contiguous), 1 the
+// warp-level mma kernel everywhere, 2 the tensor-core kernel wherever it
+// applies (also for units of up to 16 rows).
+int g_kernel_path = 0;
 thread_local int t_last_launches = 0;
 
 constexpr size_t kHeaderBytes = 256;  // error word(s)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-cudaError_t configure(int dev, const Variant& v, int* sms, int* per_sm) {
+// Sets a kernel's dynamic shared memory once per device; returns its
+// occupancy (blocks per SM) and the device's SM count.
+cudaError_t configure(int dev, const void* fn, int smem, int threads, int* sms,
+                      int* per_sm) {
   DeviceInfo& di = g_dev[dev];
   if (di.sms == 0) {
     cudaError_t e =
         cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
-  auto it = di.blocks_per_sm.find(v.fn);
+  auto it = di.blocks_per_sm.find(fn);
   if (it == di.blocks_per_sm.end()) {
     cudaError_t e = cudaFuncSetAttribute(
-        v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+        fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, v.fn, kThreads,
-                                                      v.smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
-    it = di.blocks_per_sm.emplace(v.fn, n).first;
+    it = di.blocks_per_sm.emplace(fn, n).first;
   }
   *sms = di.sms;
   *per_sm = it->second;
   return cudaSuccess;
+}
+
+cudaError_t configure(int dev, const Variant& v, int* sms, int* per_sm) {
+  return configure(dev, reinterpret_cast<const void*>(v.fn), v.smem, kThreads,
+                   sms, per_sm);
 }
 
 // Grows the stream's scratch to hold `units` counters and `part_need` bytes of
@@ -314,11 +361,16 @@ gqa_status launch(const void* q, const void* k, const void* v,
   const int NHC = (GR + kMaxUnitRows - 1) / kMaxUnitRows;
   const int R = (GR + NHC - 1) / NHC;
   const int hb = R <= 16 ? 1 : (R <= 32 ? 2 : 4);
-  const int rows_pad = hb * 16;
   const long long units = static_cast<long long>(B) * Hkv * NHC;
   if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
 
+  // the tensor-core kernel: 16-bit caches, head_dim 128, contiguous
+  const bool umma = !is_fp8(kv_kind) && D == kUmmaD && !paged &&
+                    (g_kernel_path == 2 || (g_kernel_path == 0 && R > 16));
+  const int tile_tokens = umma ? kUmmaTileTokens : kTileTokens;
+  const int rows_pad = umma ? kUmmaCols : hb * 16;
   const Variant var = pick(kv_kind, q_bf16, D, hb, R, paged);
+  const UmmaVariant uvar = umma ? umma_variant(q_bf16, R) : UmmaVariant{};
   const int elem_bytes = is_fp8(kv_kind) ? 1 : 2;
   // the TMA view [planes][rows][D]: (B*Hkv, Smax) or (num_pages*Hkv,
   // page_size)
@@ -326,19 +378,24 @@ gqa_status launch(const void* q, const void* k, const void* v,
   const int rows = paged ? page_size : Smax;
 
   std::lock_guard<std::mutex> lock(g_mu);
-  CUtensorMap map_k, map_v;
+  CUtensorMap map_k, map_v, map_q;
   if (!cached_cache_map(&map_k, k, elem_bytes, planes_outer, Hkv, rows, D) ||
       !cached_cache_map(&map_v, v, elem_bytes, planes_outer, Hkv, rows, D))
     return GQA_ERR_CUDA;
+  if (umma && !cached_q_map(&map_q, q, B * Hq * T, D)) return GQA_ERR_CUDA;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   int sms = 0, per_sm = 0;
-  if (configure(dev, var, &sms, &per_sm) != cudaSuccess) return GQA_ERR_CUDA;
+  const cudaError_t ce =
+      umma ? configure(dev, reinterpret_cast<const void*>(uvar.fn), uvar.smem,
+                       kUmmaThreads, &sms, &per_sm)
+           : configure(dev, var, &sms, &per_sm);
+  if (ce != cudaSuccess) return GQA_ERR_CUDA;
   // Default: one full wave, but never more blocks than the largest possible
   // number of tiles (seq_lens stay on the device; Smax bounds them).
   const long long max_tiles =
-      units * ((static_cast<long long>(Smax) + kTileTokens - 1) / kTileTokens);
+      units * ((static_cast<long long>(Smax) + tile_tokens - 1) / tile_tokens);
   const long long wave = static_cast<long long>(sms) * per_sm;
   const int grid = g_num_ctas_override > 0
                        ? g_num_ctas_override
@@ -377,7 +434,9 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.GR = GR;
   p.NHC = NHC;
   p.R = R;
-  p.p_align = g_num_ctas_override > 0 ? 0 : aligned_blocks(units, grid, hb);
+  p.p_align = g_num_ctas_override > 0
+                  ? 0
+                  : aligned_blocks(units, grid, umma ? 4 : hb);
   p.block_table = block_table;
   p.max_pages = paged ? Smax / page_size : 0;
   p.page_size = page_size;
@@ -388,15 +447,18 @@ gqa_status launch(const void* q, const void* k, const void* v,
   // for that kernel's completion before it reads any global memory.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = var.smem;
+  cfg.blockDim = dim3(umma ? kUmmaThreads : kThreads);
+  cfg.dynamicSmemBytes = umma ? uvar.smem : var.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, var.fn, map_k, map_v, p) != cudaSuccess) {
+  const cudaError_t le =
+      umma ? cudaLaunchKernelEx(&cfg, uvar.fn, map_k, map_v, map_q, p)
+           : cudaLaunchKernelEx(&cfg, var.fn, map_k, map_v, p);
+  if (le != cudaSuccess) {
     (void)cudaGetLastError();
     return GQA_ERR_CUDA;
   }
@@ -616,6 +678,11 @@ gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
     return GQA_ERR_CUDA;
   *flags = v;
   return GQA_OK;
+}
+
+void gqa_set_kernel_path(int path) {
+  std::lock_guard<std::mutex> lock(gqa::g_mu);
+  gqa::g_kernel_path = (path == 1 || path == 2) ? path : 0;
 }
 
 void gqa_set_wait_limit_ns(long long ns) {

@@ -222,12 +222,15 @@ __device__ __forceinline__ int clamp_len(int L, int Smax) {
   return L < 0 ? 0 : (L > Smax ? Smax : L);
 }
 
-__device__ __forceinline__ int tiles_of(int L) {
-  return (L + kTileTokens - 1) / kTileTokens;
+template <int TT>
+__device__ __forceinline__ int tiles_of_t(int L) {
+  return (L + TT - 1) / TT;
 }
 
-// Position of a block in the flat tile list, advanced one tile at a time.
-struct TileWalk {
+// Position of a block in the flat tile list (tiles of TT tokens), advanced
+// one tile at a time.
+template <int TT>
+struct TileWalkT {
   int b;          // sequence
   int L;          // its valid length
   int nt;         // its tiles per unit
@@ -245,10 +248,11 @@ struct TileWalk {
       ++b;
       if (b >= p.B) return;
       L = clamp_len(__ldg(p.seq_lens + b), p.Smax);
-      nt = tiles_of(L);
+      nt = tiles_of_t<TT>(L);
     } while (nt == 0);
   }
 };
+using TileWalk = TileWalkT<kTileTokens>;
 
 // Index of the block whose tile range holds global tile x.
 __device__ __forceinline__ int block_of_tile(long long x, long long N, int P) {
@@ -313,7 +317,8 @@ __device__ __forceinline__ void store_out8(void* out, size_t idx,
       make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Block-wide int64 sum over all kThreads threads (uses `red` scratch).
+// Block-wide int64 sum over all NT threads (uses `red` scratch).
+template <int NT>
 __device__ __forceinline__ long long block_sum(long long v, long long* red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -321,13 +326,14 @@ __device__ __forceinline__ long long block_sum(long long v, long long* red) {
   if (lane == 0) red[warp] = v;
   __syncthreads();
   long long s = 0;
-  for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+  for (int w = 0; w < NT / 32; ++w) s += red[w];
   __syncthreads();
   return s;
 }
 
-// Block-wide inclusive scan of int64 (uses `red` scratch).  Returns the
-// inclusive prefix; *total receives the block sum.
+// Block-wide inclusive scan of int64 over NT threads (uses `red` scratch).
+// Returns the inclusive prefix; *total receives the block sum.
+template <int NT>
 __device__ __forceinline__ long long block_incl_scan(long long v,
                                                      long long* red,
                                                      long long* total) {
@@ -341,7 +347,7 @@ __device__ __forceinline__ long long block_incl_scan(long long v,
   if (lane == 31) red[warp] = x;
   __syncthreads();
   long long before = 0, all = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
+  for (int w = 0; w < NT / 32; ++w) {
     if (w < warp) before += red[w];
     all += red[w];
   }
@@ -709,6 +715,98 @@ __device__ __forceinline__ uint32_t arrive_unit(const DecodeParams& p, int u) {
   return 0xffffffffu;
 }
 
+// Shared memory of plan_block.  b0, pref0 and found must be zero, and
+// visible to the whole block, before the call.
+template <int NT>
+struct PlanSmem {
+  long long red[NT / 32];
+  long long pref0;
+  int b0;
+  int found;
+};
+
+// The flat tile list (tiles of TT tokens, units sequence-major): its length
+// N, the number of blocks that take part P, this block's range [t0, t1) and
+// the walk position of its first tile.  Called by all NT threads of the
+// block.  Blocks that take part: at most one per tile (P = min(grid, N)), so
+// that every block in a unit's covering range [c_first, c_last] owns at least
+// one of its tiles (the arrival count of the split combine relies on it);
+// when every sequence has the same tile count, the host's unit-aligned count
+// p.p_align replaces it.
+template <int NT, int TT>
+__device__ __forceinline__ void plan_block(const DecodeParams& p, int HU,
+                                           PlanSmem<NT>& sm, long long& N,
+                                           int& P, long long& t0,
+                                           long long& t1, TileWalkT<TT>& w0) {
+  const int tid = threadIdx.x;
+  const int cta = blockIdx.x;
+  t0 = 0;
+  t1 = 0;
+  if (p.B <= NT) {
+    // one load of seq_lens and one block scan give everything
+    const int b = tid;
+    const int nt_b =
+        b < p.B ? tiles_of_t<TT>(clamp_len(__ldg(p.seq_lens + b), p.Smax)) : 0;
+    const int nt_0 = tiles_of_t<TT>(clamp_len(__ldg(p.seq_lens), p.Smax));
+    const long long v = static_cast<long long>(nt_b) * HU;
+    const long long incl = block_incl_scan<NT>(v, sm.red, &N);
+    // equal tile counts: the host's unit-aligned block count applies
+    const bool uniform = __syncthreads_and(b >= p.B || nt_b == nt_0) != 0;
+    P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
+    if (uniform && p.p_align > 0 && N >= p.p_align) P = p.p_align;
+    if (cta < P) {
+      t0 = N * cta / P;
+      t1 = N * (cta + 1) / P;
+    }
+    if (t0 < t1 && v > 0 && incl - v <= t0 && t0 < incl) {
+      sm.b0 = b;
+      sm.pref0 = incl - v;
+    }
+  } else {
+    long long mine = 0;
+    for (int b = tid; b < p.B; b += NT)
+      mine += static_cast<long long>(tiles_of_t<TT>(
+                  clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
+    N = block_sum<NT>(mine, sm.red);
+    P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
+    if (cta < P) {
+      t0 = N * cta / P;
+      t1 = N * (cta + 1) / P;
+    }
+    if (t0 < t1) {
+      long long run = 0;
+      for (int base = 0; base < p.B; base += NT) {
+        const int b = base + tid;
+        long long v = 0;
+        if (b < p.B)
+          v = static_cast<long long>(tiles_of_t<TT>(
+                  clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
+        long long tot;
+        const long long incl = block_incl_scan<NT>(v, sm.red, &tot);
+        const long long excl = incl - v;
+        if (v > 0 && run + excl <= t0 && t0 < run + incl) {
+          sm.b0 = b;
+          sm.pref0 = run + excl;
+          sm.found = 1;
+        }
+        run += tot;
+        __syncthreads();
+        if (sm.found) break;
+      }
+    }
+  }
+  __syncthreads();
+  if (t0 < t1) {
+    w0.b = sm.b0;
+    w0.L = clamp_len(__ldg(p.seq_lens + w0.b), p.Smax);
+    w0.nt = tiles_of_t<TT>(w0.L);
+    w0.pref = sm.pref0;
+    const long long off = t0 - w0.pref;
+    w0.j = static_cast<int>(off / w0.nt);
+    w0.ti = static_cast<int>(off % w0.nt);
+  }
+}
+
 // Warms L2 with this block's first tiles, guessing that every sequence fills
 // its cache (exact for uniform lengths; a wrong guess only costs bandwidth).
 // Uses kernel parameters only, so it may run before the previous kernel in
@@ -716,15 +814,16 @@ __device__ __forceinline__ uint32_t arrive_unit(const DecodeParams& p, int u) {
 // divide only: a 64-bit or IEEE division here compiles to a called routine
 // that costs the whole kernel registers.  The start tile only needs to be
 // close; problems with more than 2^31 tiles skip the prefetch.
-template <int KV, int D, int HB>
+template <int KV, int D, int HB, int TT = kTileTokens>
 __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
                                                      const CUtensorMap* map_v,
                                                      int B, int Hkv, int NHC,
                                                      int Smax, int p_align,
                                                      int lane) {
   using C = Cfg<KV, D, HB>;
-  const unsigned nt = (static_cast<unsigned>(Smax) + kTileTokens - 1) /
-                      kTileTokens;
+  // the same bytes whatever the tile length: kPrefetchTiles 64-token tiles
+  constexpr int kTiles = kPrefetchTiles * kTileTokens / TT;
+  const unsigned nt = (static_cast<unsigned>(Smax) + TT - 1) / TT;
   const unsigned long long n64 =
       static_cast<unsigned long long>(nt) * Hkv * NHC * B;
   if (n64 == 0ull || n64 > 0x7fffffffull) return;
@@ -739,16 +838,20 @@ __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
   // lane k prefetches tile k of the range (one warp, no divergence in the
   // arithmetic)
   x0 += lane;
-  if (lane < kPrefetchTiles && x0 < ng) {
+  if (lane < kTiles && x0 < ng) {
     const unsigned bq = x0 / per_seq, rem = x0 % per_seq;
     const int plane = static_cast<int>(bq) * Hkv +
                       static_cast<int>(rem / nt) / NHC;
-    const int tok = static_cast<int>(rem % nt) * kTileTokens;
+    const int tok = static_cast<int>(rem % nt) * TT;
 #pragma unroll
-    for (int bx = 0; bx < C::kBoxesPerTile; ++bx) {
-      ptx::tma_prefetch_3d(map_k, bx * C::kBoxElems, tok, plane);
-      ptx::tma_prefetch_3d(map_v, bx * C::kBoxElems, tok, plane);
-    }
+    for (int th = 0; th < TT / kTileTokens; ++th)
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxesPerTile; ++bx) {
+        ptx::tma_prefetch_3d(map_k, bx * C::kBoxElems, tok + th * kTileTokens,
+                             plane);
+        ptx::tma_prefetch_3d(map_v, bx * C::kBoxElems, tok + th * kTileTokens,
+                             plane);
+      }
   }
 }
 
@@ -778,10 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + C::kStages;
   uint64_t* dump_full = empty + C::kStages;   // 8 consumer warps arrive
   uint64_t* dump_empty = dump_full + 1;       // the merge warps arrive
-  __shared__ long long s_red[kThreads / 32];
-  __shared__ long long s_pref0;
-  __shared__ int s_b0;
-  __shared__ int s_found;
+  __shared__ PlanSmem<kThreads> s_plan;
   __shared__ volatile int s_abort;
   // the flat list's tile count and the blocks taking part, re-read at unit
   // ends (volatile: not held in registers through the tile loop)
@@ -824,9 +924,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_barrier_init();
     s_abort = 0;
     s_npend = 0;
-    s_found = 0;
-    s_b0 = 0;
-    s_pref0 = 0;
+    s_plan.found = 0;
+    s_plan.b0 = 0;
+    s_plan.pref0 = 0;
   }
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: everything above overlapped its tail; nothing before this point
@@ -835,80 +935,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::griddep_launch_dependents();
 
   // ---- flat tile list: total N, this block's range, its first sequence ----
-  // Blocks that take part: at most one per tile (P = min(grid, N)), so that
-  // every block in a unit's covering range [c_first, c_last] owns at least
-  // one of its tiles (the arrival count of the split combine relies on it).
-  long long N, t0 = 0, t1 = 0;
+  long long N, t0, t1;
   int P;
-  if (p.B <= kThreads) {
-    // one load of seq_lens and one block scan give everything
-    const int b = tid;
-    const int nt_b =
-        b < p.B ? tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax)) : 0;
-    const int nt_0 = tiles_of(clamp_len(__ldg(p.seq_lens), p.Smax));
-    const long long v = static_cast<long long>(nt_b) * HU;
-    const long long incl = block_incl_scan(v, s_red, &N);
-    // equal tile counts: the host's unit-aligned block count applies
-    const bool uniform = __syncthreads_and(b >= p.B || nt_b == nt_0) != 0;
-    P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
-    if (uniform && p.p_align > 0 && N >= p.p_align) P = p.p_align;
-    if (cta < P) {
-      t0 = N * cta / P;
-      t1 = N * (cta + 1) / P;
-    }
-    if (t0 < t1 && v > 0 && incl - v <= t0 && t0 < incl) {
-      s_b0 = b;
-      s_pref0 = incl - v;
-    }
-  } else {
-    long long mine = 0;
-    for (int b = tid; b < p.B; b += kThreads)
-      mine += static_cast<long long>(
-                  tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
-    N = block_sum(mine, s_red);
-    P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
-    if (cta < P) {
-      t0 = N * cta / P;
-      t1 = N * (cta + 1) / P;
-    }
-    if (t0 < t1) {
-      long long run = 0;
-      for (int base = 0; base < p.B; base += kThreads) {
-        const int b = base + tid;
-        long long v = 0;
-        if (b < p.B)
-          v = static_cast<long long>(
-                  tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
-        long long tot;
-        const long long incl = block_incl_scan(v, s_red, &tot);
-        const long long excl = incl - v;
-        if (v > 0 && run + excl <= t0 && t0 < run + incl) {
-          s_b0 = b;
-          s_pref0 = run + excl;
-          s_found = 1;
-        }
-        run += tot;
-        __syncthreads();
-        if (s_found) break;
-      }
-    }
-  }
+  TileWalk w0;
+  plan_block<kThreads, kTileTokens>(p, HU, s_plan, N, P, t0, t1, w0);
   if (tid == 0) {
     s_N = N;
     s_P = P;
   }
   __syncthreads();
-
-  TileWalk w0;
-  if (t0 < t1) {
-    w0.b = s_b0;
-    w0.L = clamp_len(__ldg(p.seq_lens + w0.b), p.Smax);
-    w0.nt = tiles_of(w0.L);
-    w0.pref = s_pref0;
-    const long long off = t0 - w0.pref;
-    w0.j = static_cast<int>(off / w0.nt);
-    w0.ti = static_cast<int>(off % w0.nt);
-  }
 
   if (warp < 4) {
     ptx::setmaxnreg_dec<kRegsSmall>();

@@ -29,6 +29,11 @@ Recipe (all on the host, torch CPU generator seeded per workload):
    (1 when the absmax is 0), then ``(x / scale)`` cast to float8_e4m3fn.
 4. cache positions t >= seq_lens[b] are filled with ``pad``: NaN (so that a
    kernel that reads past the valid prefix poisons its output) or zero.
+
+The same recipe can run on a CUDA device (``device=``), with torch's CUDA
+generator seeded the same way: same shapes and distributions, different
+draws.  The benchmark uses it to set up large workloads quickly; the parity
+tests draw on the host.
 """
 from __future__ import annotations
 
@@ -134,20 +139,23 @@ HEADLINE = "llama70b_b8_s8192_bf16"
 
 
 def draw_seq_lens(w: Workload, gen: torch.Generator) -> torch.Tensor:
+    """seq_lens [B] int32, on the generator's device."""
     kind = w.lens[0]
+    dev = gen.device
     if kind == "uniform":
-        return torch.full((w.B,), w.Smax, dtype=torch.int32)
+        return torch.full((w.B,), w.Smax, dtype=torch.int32, device=dev)
     if kind == "fixed":
-        return torch.full((w.B,), int(w.lens[1]), dtype=torch.int32)
+        return torch.full((w.B,), int(w.lens[1]), dtype=torch.int32,
+                          device=dev)
     if kind == "ragged":
         lo, hi = int(w.lens[1]), int(w.lens[2])
         return torch.randint(lo, hi + 1, (w.B,), generator=gen,
-                             dtype=torch.int64).to(torch.int32)
+                             dtype=torch.int64, device=dev).to(torch.int32)
     if kind == "list":
         vals = [int(x) for x in w.lens[1:]]
         if len(vals) != w.B:
             raise ValueError("('list', ...) needs one length per sequence")
-        return torch.tensor(vals, dtype=torch.int32)
+        return torch.tensor(vals, dtype=torch.int32, device=dev)
     raise ValueError(f"unknown length mix {w.lens!r}")
 
 
@@ -160,20 +168,23 @@ def _pad_value(dtype: torch.dtype, pad: str):
 
 
 def make_inputs(w: Workload, *, pad: str = "nan",
-                seed: Optional[int] = None) -> dict:
-    """Host (CPU) tensors for one decode step of workload ``w``.
+                seed: Optional[int] = None, device=None) -> dict:
+    """Tensors for one decode step of workload ``w``, on the host (default)
+    or drawn directly on ``device``.
 
     Returns a dict with ``q`` [B,Hq,D], ``k``/``v`` [B,Hkv,Smax,D] (q dtype, or
     float8_e4m3fn for the FP8 cache), ``k_scale``/``v_scale`` [B,Hkv] float32
     (FP8 only, else None), ``seq_lens`` [B] int32 and ``scale`` (1/sqrt(D)).
     """
-    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    dev = torch.device(device) if device is not None else torch.device("cpu")
+    gen = torch.Generator(device=dev).manual_seed(
+        w.seed if seed is None else seed)
     seq_lens = draw_seq_lens(w, gen)
     if w.B > 0 and int(seq_lens.max()) > w.Smax:
         raise ValueError("a sequence is longer than the cache")
     qdt = _DT[w.dtype]
     qshape = (w.B, w.Hq, w.D) if w.T == 1 else (w.B, w.Hq, w.T, w.D)
-    q = torch.randn(qshape, generator=gen).to(qdt)
+    q = torch.randn(qshape, generator=gen, device=dev).to(qdt)
 
     fp8 = w.kv in _FP8
     if fp8:
@@ -182,21 +193,22 @@ def make_inputs(w: Workload, *, pad: str = "nan",
         cdt = qdt
     shape = (w.B, w.Hkv, w.Smax, w.D)
     if fp8:
-        k = torch.empty(shape, dtype=torch.uint8)
-        v = torch.empty(shape, dtype=torch.uint8)
-        k_scale = torch.ones((w.B, w.Hkv), dtype=torch.float32)
-        v_scale = torch.ones((w.B, w.Hkv), dtype=torch.float32)
+        k = torch.empty(shape, dtype=torch.uint8, device=dev)
+        v = torch.empty(shape, dtype=torch.uint8, device=dev)
+        k_scale = torch.ones((w.B, w.Hkv), dtype=torch.float32, device=dev)
+        v_scale = torch.ones((w.B, w.Hkv), dtype=torch.float32, device=dev)
         k.fill_(nan_code if pad == "nan" else 0)
         v.fill_(nan_code if pad == "nan" else 0)
     else:
-        k = torch.full(shape, _pad_value(qdt, pad), dtype=cdt)
-        v = torch.full(shape, _pad_value(qdt, pad), dtype=cdt)
+        k = torch.full(shape, _pad_value(qdt, pad), dtype=cdt, device=dev)
+        v = torch.full(shape, _pad_value(qdt, pad), dtype=cdt, device=dev)
         k_scale = v_scale = None
 
+    lens_host = seq_lens.cpu()
     for b in range(w.B):
-        L = int(seq_lens[b])
+        L = int(lens_host[b])
         for name, dst, sc in (("k", k, k_scale), ("v", v, v_scale)):
-            x = torch.randn((w.Hkv, L, w.D), generator=gen)
+            x = torch.randn((w.Hkv, L, w.D), generator=gen, device=dev)
             if L == 0:
                 continue
             if fp8:
@@ -224,31 +236,34 @@ def to_pages(k, v, seq_lens, page_size: int, gen: torch.Generator,
     [num_pages, Hkv, page_size, D] with a block table [B, max_pages] (int32,
     -1 where a sequence has no page).  A few spare pages hold the pad value."""
     B, Hkv, Smax, D = k.shape
+    dev = k.device
     max_pages = -(-Smax // page_size)
     num_pages = B * max_pages + max(2, B)
-    perm = torch.randperm(num_pages, generator=gen)[:B * max_pages]
-    perm = perm.view(B, max_pages).to(torch.int32)
+    perm = torch.randperm(num_pages, generator=gen,
+                          device=gen.device)[:B * max_pages]
+    perm = perm.view(B, max_pages).to(torch.int32).cpu()
     fill = _pad_value(k.dtype, pad) if k.dtype.itemsize == 2 else None
     shape = (num_pages, Hkv, page_size, D)
     if fill is None:   # 8-bit codes: fill through a byte view
-        kp = torch.zeros(shape, dtype=torch.uint8)
-        vp = torch.zeros(shape, dtype=torch.uint8)
+        kp = torch.zeros(shape, dtype=torch.uint8, device=dev)
+        vp = torch.zeros(shape, dtype=torch.uint8, device=dev)
         kp.fill_(0x7F if pad == "nan" else 0)
         vp.fill_(0x7F if pad == "nan" else 0)
         kp, vp = kp.view(k.dtype), vp.view(k.dtype)
     else:
-        kp = torch.full(shape, fill, dtype=k.dtype)
-        vp = torch.full(shape, fill, dtype=k.dtype)
+        kp = torch.full(shape, fill, dtype=k.dtype, device=dev)
+        vp = torch.full(shape, fill, dtype=k.dtype, device=dev)
     table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    lens_host = seq_lens.cpu()
     for b in range(B):
-        n = -(-int(seq_lens[b]) // page_size)
+        n = -(-int(lens_host[b]) // page_size)
         for i in range(n):
             pg = int(perm[b, i])
             lo, hi = i * page_size, min((i + 1) * page_size, Smax)
             kp[pg, :, :hi - lo] = k[b, :, lo:hi]
             vp[pg, :, :hi - lo] = v[b, :, lo:hi]
             table[b, i] = pg
-    return {"k": kp, "v": vp, "block_table": table, "k_contig": k,
+    return {"k": kp, "v": vp, "block_table": table.to(dev), "k_contig": k,
             "v_contig": v}
 
 

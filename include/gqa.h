@@ -276,6 +276,19 @@ const char* gqa_status_string(gqa_status status);
 gqa_status gqa_device_errors(void* stream, uint32_t* flags);
 
 /*
+ * gqa_set_kernel_path — test and tuning hook: which kernel the decode calls
+ * launch (process-wide; host only).  0 (the default): the tensor-core kernel
+ * (fifth-generation tensor core, accumulators in tensor memory) for units of
+ * more than 16 query rows per KV head with a 16-bit cache, head_dim 128 and
+ * a contiguous cache (multi-query attention, wide groups, multi-token
+ * chunks), the warp-level mma kernel otherwise.  1: the warp-level kernel
+ * everywhere.  2: the tensor-core kernel wherever it applies, units of up to
+ * 16 rows included.  The result is the same within the stated tolerance
+ * (fp32 accumulation both ways); other values count as 0.
+ */
+void gqa_set_kernel_path(int path);
+
+/*
  * gqa_set_wait_limit_ns — test hook: the time limit of every pipeline wait in
  * the decode kernels launched afterwards (process-wide; host only).  A wait
  * that runs out sets bit 0 of gqa_device_errors, and the kernel stops waiting
