@@ -504,6 +504,31 @@ def bench_append(a, w, name, peak, peak_kind):
     return 0
 
 
+def profile_launches(w, name, dev, n: int) -> int:
+    """Profiling mode: the workload's inputs drawn on the device, then n
+    decode launches back to back and nothing else, for a profiler to capture
+    (``-s`` skips the first ones)."""
+    import torch
+    import grouped_query_attention_11_b300 as gq
+    from grouped_query_attention_11_b300.workloads import make_inputs
+    inp = make_inputs(w, pad="zero", device=dev)
+    inp.pop("k_contig", None)
+    inp.pop("v_contig", None)
+    out = torch.empty_like(inp["q"])
+    stream = torch.cuda.current_stream()
+    step = gq.BoundDecode(inp, out, stream)
+    torch.cuda.synchronize()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    err = gq.gqa_device_errors(stream)
+    print(json.dumps({"profile_launches": n, "workload": name,
+                      "device_errors": err,
+                      "launches_per_step": gq.gqa_last_launch_count()}),
+          flush=True)
+    return 0 if err == 0 else 1
+
+
 def job_us_per_step(us: float, ws: int, device) -> float:
     """Whole-job time per step of ws replicas that each ran the same steps:
     the slowest rank's time (max over ranks, one all-reduce on the timing
@@ -538,6 +563,15 @@ def main(argv=None):
     ap.add_argument("--op", default="decode", choices=["decode", "append"],
                     help="decode: the decode step (default); append: the "
                          "cache-append step before it")
+    ap.add_argument("--kernel-path", type=int, default=0, choices=[0, 1, 2],
+                    help="0 automatic kernel choice (default); 1 the "
+                         "warp-level mma kernel only; 2 the tensor-core "
+                         "kernel wherever it applies (for A/B comparisons)")
+    ap.add_argument("--profile-launches", type=int, default=0,
+                    help="profiling mode: build the workload's inputs, "
+                         "launch exactly this many decode steps, check the "
+                         "error flags and exit (no timing, no other "
+                         "kernels after the inputs are drawn)")
     a = ap.parse_args(argv)
 
     from grouped_query_attention_11_b300.workloads import (HEADLINE,
@@ -599,6 +633,12 @@ def main(argv=None):
     dev = torch.device("cuda", torch.cuda.current_device())
     gq.lib()
     gq.gqa_set_num_ctas(0)
+    gq.gqa_set_kernel_path(a.kernel_path)
+    cfg["kernel_path"] = ("automatic", "warp-level mma",
+                          "tensor core where it applies")[a.kernel_path]
+
+    if a.profile_launches > 0:
+        return profile_launches(w, name, dev, a.profile_launches)
 
     inp = make_inputs(w, pad="zero", seed=w.seed + rank)
     # a paged workload also carries its contiguous copy (for checks): not an

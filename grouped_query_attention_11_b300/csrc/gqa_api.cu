@@ -253,6 +253,33 @@ cudaError_t configure(int dev, const void* fn, int smem, int threads, int* sms,
   return cudaSuccess;
 }
 
+// How many clusters of k blocks of kernel `fn` can run at the same time on
+// the device (cached per kernel and k; 0 when the query fails).
+long long max_clusters(int dev, const void* fn, int smem, int threads, int k) {
+  static std::map<std::tuple<int, const void*, int>, long long> cache;
+  const auto key = std::make_tuple(dev, fn, k);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(k));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(k);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache.emplace(key, n);
+  return n;
+}
+
 cudaError_t configure(int dev, const Variant& v, int* sms, int* per_sm) {
   return configure(dev, reinterpret_cast<const void*>(v.fn), v.smem, kThreads,
                    sms, per_sm);
@@ -364,13 +391,14 @@ gqa_status launch(const void* q, const void* k, const void* v,
   const long long units = static_cast<long long>(B) * Hkv * NHC;
   if (units > INT32_MAX / 2) return GQA_ERR_UNSUPPORTED;
 
-  // the tensor-core kernel: 16-bit caches, head_dim 128, contiguous
-  const bool umma = !is_fp8(kv_kind) && D == kUmmaD && !paged &&
+  // the tensor-core kernel: 16-bit caches, head_dim 128
+  const bool umma = !is_fp8(kv_kind) && D == kUmmaD &&
                     (g_kernel_path == 2 || (g_kernel_path == 0 && R > 16));
   const int tile_tokens = umma ? kUmmaTileTokens : kTileTokens;
   const int rows_pad = umma ? kUmmaCols : hb * 16;
   const Variant var = pick(kv_kind, q_bf16, D, hb, R, paged);
-  const UmmaVariant uvar = umma ? umma_variant(q_bf16, R) : UmmaVariant{};
+  const UmmaVariant uvar = umma ? umma_variant(q_bf16, R, paged)
+                                : UmmaVariant{};
   const int elem_bytes = is_fp8(kv_kind) ? 1 : 2;
   // the TMA view [planes][rows][D]: (B*Hkv, Smax) or (num_pages*Hkv,
   // page_size)
@@ -397,9 +425,25 @@ gqa_status launch(const void* q, const void* k, const void* v,
   const long long max_tiles =
       units * ((static_cast<long long>(Smax) + tile_tokens - 1) / tile_tokens);
   const long long wave = static_cast<long long>(sms) * per_sm;
-  const int grid = g_num_ctas_override > 0
-                       ? g_num_ctas_override
-                       : static_cast<int>(max_tiles < wave ? max_tiles : wave);
+  int grid = g_num_ctas_override > 0
+                 ? g_num_ctas_override
+                 : static_cast<int>(max_tiles < wave ? max_tiles : wave);
+  const int p_align = g_num_ctas_override > 0
+                          ? 0
+                          : aligned_blocks(units, grid, umma ? 4 : hb);
+  // Tensor-core kernel, every unit split evenly over k = 2 or 4 blocks:
+  // launch those blocks as thread-block clusters, which merge their states
+  // through distributed shared memory, when every cluster fits at once.
+  int cluster = 0;
+  if (umma && p_align > units && p_align % units == 0) {
+    const int k = static_cast<int>(p_align / units);
+    if ((k == 2 || k == 4) &&
+        max_clusters(dev, reinterpret_cast<const void*>(uvar.fn), uvar.smem,
+                     kUmmaThreads, k) >= units) {
+      cluster = k;
+      grid = p_align;
+    }
+  }
 
   const size_t slots = static_cast<size_t>(grid) + static_cast<size_t>(units);
   const size_t lse_bytes = align_up(slots * rows_pad * 4, 256);
@@ -434,9 +478,8 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.GR = GR;
   p.NHC = NHC;
   p.R = R;
-  p.p_align = g_num_ctas_override > 0
-                  ? 0
-                  : aligned_blocks(units, grid, umma ? 4 : hb);
+  p.p_align = p_align;
+  p.cluster = cluster;
   p.block_table = block_table;
   p.max_pages = paged ? Smax / page_size : 0;
   p.page_size = page_size;
@@ -450,11 +493,18 @@ gqa_status launch(const void* q, const void* k, const void* v,
   cfg.blockDim = dim3(umma ? kUmmaThreads : kThreads);
   cfg.dynamicSmemBytes = umma ? uvar.smem : var.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   const cudaError_t le =
       umma ? cudaLaunchKernelEx(&cfg, uvar.fn, map_k, map_v, map_q, p)
            : cudaLaunchKernelEx(&cfg, var.fn, map_k, map_v, p);

@@ -153,6 +153,11 @@ struct DecodeParams {
   // by the host so that block ranges line up with unit boundaries (0: none;
   // then min(grid, tiles) blocks take part).
   int p_align;
+  // Tensor-core kernel only: the launch's cluster size when p_align splits
+  // every unit evenly over the CTAs of one thread-block cluster (2 or 4);
+  // their states are then merged through distributed shared memory.  0 or
+  // 1: no cluster launch.
+  int cluster;
 };
 
 // ------------------------------------------------------------ compile-time

@@ -4,15 +4,23 @@
 
 namespace gqa {
 
-UmmaVariant umma_variant(bool q_bf16, int rows) {
-  if (q_bf16)
-    return rows <= 32 ? UmmaVariant{&gqa_decode_umma_kernel<true, 32>,
-                                    kUmmaSmemBytes}
-                      : UmmaVariant{&gqa_decode_umma_kernel<true, 64>,
-                                    kUmmaSmemBytes};
+namespace {
+
+template <bool QBF16, bool PAGED>
+UmmaVariant pick_cols(int rows) {
   return rows <= 32
-             ? UmmaVariant{&gqa_decode_umma_kernel<false, 32>, kUmmaSmemBytes}
-             : UmmaVariant{&gqa_decode_umma_kernel<false, 64>, kUmmaSmemBytes};
+             ? UmmaVariant{&gqa_decode_umma_kernel<QBF16, 32, PAGED>,
+                           kUmmaSmemBytes}
+             : UmmaVariant{&gqa_decode_umma_kernel<QBF16, 64, PAGED>,
+                           kUmmaSmemBytes};
+}
+
+}  // namespace
+
+UmmaVariant umma_variant(bool q_bf16, int rows, bool paged) {
+  if (q_bf16)
+    return paged ? pick_cols<true, true>(rows) : pick_cols<true, false>(rows);
+  return paged ? pick_cols<false, true>(rows) : pick_cols<false, false>(rows);
 }
 
 }  // namespace gqa

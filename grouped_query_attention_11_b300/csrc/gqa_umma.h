@@ -18,8 +18,9 @@ struct UmmaVariant {
   int smem;  // dynamic shared memory per block
 };
 
-// The instantiation for q / out in bf16 (else f16) and units of `rows` query
-// rows (17 .. 64; up to 32 use the 32-column softmax).
-UmmaVariant umma_variant(bool q_bf16, int rows);
+// The instantiation for q / out in bf16 (else f16), units of `rows` query
+// rows (17 .. 64; up to 32 use the 32-column softmax) and a contiguous or
+// paged cache.
+UmmaVariant umma_variant(bool q_bf16, int rows, bool paged);
 
 }  // namespace gqa
