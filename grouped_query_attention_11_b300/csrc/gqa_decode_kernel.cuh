@@ -72,6 +72,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
@@ -720,15 +721,36 @@ __device__ __forceinline__ uint32_t arrive_unit(const DecodeParams& p, int u) {
   return 0xffffffffu;
 }
 
-// Shared memory of plan_block.  b0, pref0 and found must be zero, and
+// Shared memory of plan_block.  b0, L0, pref0 and found must be zero, and
 // visible to the whole block, before the call.
+// Warms L2 with the lines of seq_lens (read first after the wait for the
+// previous kernel; an L2 prefetch returns nothing to the thread, so it may be
+// issued before that wait).  Threads 0..31 of the block.
+__device__ __forceinline__ void prefetch_seq_lens(const DecodeParams& p,
+                                                  int tid) {
+  if (tid < 32 && tid * 32 < p.B) ptx::prefetch_l2(p.seq_lens + tid * 32);
+}
+
 template <int NT>
 struct PlanSmem {
   long long red[NT / 32];
+  int nt_min[NT / 32], nt_max[NT / 32];
   long long pref0;
   int b0;
+  int L0;
   int found;
 };
+
+// floor(N * c / P) for the block-range edges: 32-bit unsigned division when
+// the product fits (the common case), else 64-bit.
+__device__ __forceinline__ long long range_edge(long long N, int c, int P) {
+  const unsigned long long x = static_cast<unsigned long long>(N) *
+                               static_cast<unsigned>(c);
+  if (x <= 0xffffffffull)
+    return static_cast<long long>(static_cast<unsigned>(x) /
+                                  static_cast<unsigned>(P));
+  return static_cast<long long>(x / static_cast<unsigned long long>(P));
+}
 
 // The flat tile list (tiles of TT tokens, units sequence-major): its length
 // N, the number of blocks that take part P, this block's range [t0, t1) and
@@ -738,6 +760,10 @@ struct PlanSmem {
 // one of its tiles (the arrival count of the split combine relies on it);
 // when every sequence has the same tile count, the host's unit-aligned count
 // p.p_align replaces it.
+//
+// Batches of at most NT sequences: one seq_lens load per thread, a warp scan
+// and two block barriers (the warps' totals and tile-count extremes, then the
+// block's start position).
 template <int NT, int TT>
 __device__ __forceinline__ void plan_block(const DecodeParams& p, int HU,
                                            PlanSmem<NT>& sm, long long& N,
@@ -748,24 +774,49 @@ __device__ __forceinline__ void plan_block(const DecodeParams& p, int HU,
   t0 = 0;
   t1 = 0;
   if (p.B <= NT) {
-    // one load of seq_lens and one block scan give everything
     const int b = tid;
-    const int nt_b =
-        b < p.B ? tiles_of_t<TT>(clamp_len(__ldg(p.seq_lens + b), p.Smax)) : 0;
-    const int nt_0 = tiles_of_t<TT>(clamp_len(__ldg(p.seq_lens), p.Smax));
+    const int warp = tid >> 5, lane = tid & 31;
+    const int Lb = b < p.B ? clamp_len(__ldg(p.seq_lens + b), p.Smax) : 0;
+    const int nt_b = tiles_of_t<TT>(Lb);
     const long long v = static_cast<long long>(nt_b) * HU;
-    const long long incl = block_incl_scan<NT>(v, sm.red, &N);
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const int wmin = __reduce_min_sync(0xffffffffu, b < p.B ? nt_b : INT_MAX);
+    const int wmax = __reduce_max_sync(0xffffffffu, b < p.B ? nt_b : 0);
+    if (lane == 31) {
+      sm.red[warp] = x;
+      sm.nt_min[warp] = wmin;
+      sm.nt_max[warp] = wmax;
+    }
+    __syncthreads();
+    long long before = 0;
+    N = 0;
+    int mn = INT_MAX, mx = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+      const long long r = sm.red[w];
+      before += w < warp ? r : 0;
+      N += r;
+      mn = min(mn, sm.nt_min[w]);
+      mx = max(mx, sm.nt_max[w]);
+    }
+    const long long incl = before + x;
     // equal tile counts: the host's unit-aligned block count applies
-    const bool uniform = __syncthreads_and(b >= p.B || nt_b == nt_0) != 0;
+    const bool uniform = mn == mx;
     P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
     if (uniform && p.p_align > 0 && N >= p.p_align) P = p.p_align;
     if (cta < P) {
-      t0 = N * cta / P;
-      t1 = N * (cta + 1) / P;
+      t0 = range_edge(N, cta, P);
+      t1 = range_edge(N, cta + 1, P);
     }
     if (t0 < t1 && v > 0 && incl - v <= t0 && t0 < incl) {
       sm.b0 = b;
       sm.pref0 = incl - v;
+      sm.L0 = Lb;
     }
   } else {
     long long mine = 0;
@@ -775,23 +826,26 @@ __device__ __forceinline__ void plan_block(const DecodeParams& p, int HU,
     N = block_sum<NT>(mine, sm.red);
     P = static_cast<int>(N < gridDim.x ? N : gridDim.x);
     if (cta < P) {
-      t0 = N * cta / P;
-      t1 = N * (cta + 1) / P;
+      t0 = range_edge(N, cta, P);
+      t1 = range_edge(N, cta + 1, P);
     }
     if (t0 < t1) {
       long long run = 0;
       for (int base = 0; base < p.B; base += NT) {
         const int b = base + tid;
         long long v = 0;
-        if (b < p.B)
-          v = static_cast<long long>(tiles_of_t<TT>(
-                  clamp_len(__ldg(p.seq_lens + b), p.Smax))) * HU;
+        int Lb = 0;
+        if (b < p.B) {
+          Lb = clamp_len(__ldg(p.seq_lens + b), p.Smax);
+          v = static_cast<long long>(tiles_of_t<TT>(Lb)) * HU;
+        }
         long long tot;
         const long long incl = block_incl_scan<NT>(v, sm.red, &tot);
         const long long excl = incl - v;
         if (v > 0 && run + excl <= t0 && t0 < run + incl) {
           sm.b0 = b;
           sm.pref0 = run + excl;
+          sm.L0 = Lb;
           sm.found = 1;
         }
         run += tot;
@@ -803,12 +857,19 @@ __device__ __forceinline__ void plan_block(const DecodeParams& p, int HU,
   __syncthreads();
   if (t0 < t1) {
     w0.b = sm.b0;
-    w0.L = clamp_len(__ldg(p.seq_lens + w0.b), p.Smax);
+    w0.L = sm.L0;
     w0.nt = tiles_of_t<TT>(w0.L);
     w0.pref = sm.pref0;
     const long long off = t0 - w0.pref;
-    w0.j = static_cast<int>(off / w0.nt);
-    w0.ti = static_cast<int>(off % w0.nt);
+    if (off <= 0x7fffffffll) {
+      const unsigned uo = static_cast<unsigned>(off);
+      const unsigned jj = uo / static_cast<unsigned>(w0.nt);
+      w0.j = static_cast<int>(jj);
+      w0.ti = static_cast<int>(uo - jj * static_cast<unsigned>(w0.nt));
+    } else {
+      w0.j = static_cast<int>(off / w0.nt);
+      w0.ti = static_cast<int>(off % w0.nt);
+    }
   }
 }
 
@@ -931,11 +992,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_npend = 0;
     s_plan.found = 0;
     s_plan.b0 = 0;
+    s_plan.L0 = 0;
     s_plan.pref0 = 0;
   }
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: everything above overlapped its tail; nothing before this point
   // reads global memory (q, the caches and seq_lens may be written by it).
+  // seq_lens is only warmed in L2, which stays coherent with those writes.
+  prefetch_seq_lens(p, tid);
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 

@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     s_npend = 0;
     s_plan.found = 0;
     s_plan.b0 = 0;
+    s_plan.L0 = 0;
     s_plan.pref0 = 0;
   }
   if (warp == 1) {
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  prefetch_seq_lens(p, tid);
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
@@ -775,18 +777,28 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       const int row = static_cast<int>(rank) * rpc + i / kG;
       const int n = i % kG;
       if (row >= Rv) continue;
+      // every CTA's values first (independent loads in flight together),
+      // then the arithmetic
       float mv[4], lv[4];
-      float M = -INFINITY;
+      float4 ov[4][2];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        mv[r] = -INFINITY;
-        lv[r] = 0.f;
         if (r < k) {
+          const uint32_t a =
+              ptx::mapa_shared(o_s + (row * D + 8 * n) * 4, r);
           mv[r] = ptx::ld_dsmem_f32(ptx::mapa_shared(m_s + row * 4, r));
           lv[r] = ptx::ld_dsmem_f32(ptx::mapa_shared(l_s + row * 4, r));
+          ov[r][0] = ptx::ld_dsmem_f4(a);
+          ov[r][1] = ptx::ld_dsmem_f4(a + 16);
+        } else {
+          mv[r] = -INFINITY;
+          lv[r] = 0.f;
+          ov[r][0] = ov[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        M = fmaxf(M, mv[r]);
       }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) M = fmaxf(M, mv[r]);
       float acc[8];
 #pragma unroll
       for (int x = 0; x < 8; ++x) acc[x] = 0.f;
@@ -794,21 +806,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       if (M != -INFINITY) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          if (r >= k || mv[r] == -INFINITY) continue;
+          if (mv[r] == -INFINITY) continue;
           const float f = ptx::ex2(mv[r] - M);
           lt += f * lv[r];
-          const uint32_t a =
-              ptx::mapa_shared(o_s + (row * D + 8 * n) * 4, r);
-          const float4 v0 = ptx::ld_dsmem_f4(a);
-          const float4 v1 = ptx::ld_dsmem_f4(a + 16);
-          acc[0] += f * v0.x;
-          acc[1] += f * v0.y;
-          acc[2] += f * v0.z;
-          acc[3] += f * v0.w;
-          acc[4] += f * v1.x;
-          acc[5] += f * v1.y;
-          acc[6] += f * v1.z;
-          acc[7] += f * v1.w;
+          acc[0] += f * ov[r][0].x;
+          acc[1] += f * ov[r][0].y;
+          acc[2] += f * ov[r][0].z;
+          acc[3] += f * ov[r][0].w;
+          acc[4] += f * ov[r][1].x;
+          acc[5] += f * ov[r][1].y;
+          acc[6] += f * ov[r][1].z;
+          acc[7] += f * ov[r][1].w;
         }
       }
       store_out8<QBF16>(p.out, (rbase + row) * D + 8 * n, acc,

@@ -129,6 +129,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0,
       : "memory");
 }
 
+// Warms L2 with the 128-byte line holding `ptr` (no data returned).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
