@@ -567,6 +567,9 @@ def main(argv=None):
                     help="0 automatic kernel choice (default); 1 the "
                          "warp-level mma kernel only; 2 the tensor-core "
                          "kernel wherever it applies (for A/B comparisons)")
+    ap.add_argument("--num-ctas", type=int, default=0,
+                    help="blocks per launch (0: the library's own choice, "
+                         "the default; for A/B comparisons of the split)")
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="profiling mode: build the workload's inputs, "
                          "launch exactly this many decode steps, check the "
@@ -632,8 +635,10 @@ def main(argv=None):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
     gq.lib()
-    gq.gqa_set_num_ctas(0)
+    gq.gqa_set_num_ctas(a.num_ctas)
     gq.gqa_set_kernel_path(a.kernel_path)
+    if a.num_ctas:
+        cfg["num_ctas"] = a.num_ctas
     cfg["kernel_path"] = ("automatic", "warp-level mma",
                           "tensor core where it applies")[a.kernel_path]
 

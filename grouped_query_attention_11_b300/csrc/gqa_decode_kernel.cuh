@@ -107,6 +107,9 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s per final drain
 // Retries of the compare-and-swap that counts a block's arrival at a unit
 // (each failure means another block's arrival succeeded, so a few suffice).
 constexpr int kMaxArrivalTries = 1 << 16;
+constexpr int kQPrefetchUnits = 8;   // later units whose q rows are warmed
+// A split-combine ticket not yet returned by the arrival (never a count).
+constexpr uint32_t kTicketPending = 0xfffffffeu;
 // Dynamic shared memory per block: the sm_100-family opt-in maximum (227 KB)
 // less 512 bytes left for the kernel's static shared variables.
 constexpr int kSmemBudget = 232448 - 512;
@@ -703,17 +706,22 @@ __device__ __forceinline__ void combine_unit(int t, const DecodeParams& p,
 // as no arrival, so such a launch cannot shift the tickets of later ones.
 // The swap has acquire-release semantics: the caller's partial stores (and
 // those ordered before it by a barrier) are released, and the last arriver
-// sees every other block's.  Sets kErrWaitTimeout and returns a ticket that
-// matches no arrival count if the swap keeps failing.
-__device__ __forceinline__ uint32_t arrive_unit(const DecodeParams& p, int u) {
+// sees every other block's.  The first swap guesses that this block is the
+// last of the unit's `expect` blocks (one round trip for the block that then
+// combines, which is the one on the kernel's critical path); a wrong guess
+// returns the counter's value for the next try.  Sets kErrWaitTimeout and
+// returns a ticket that matches no arrival count if the swap keeps failing.
+__device__ __forceinline__ uint32_t arrive_unit(const DecodeParams& p, int u,
+                                                int expect) {
   unsigned long long* c = p.counters + u;
   const unsigned long long tag = static_cast<unsigned long long>(p.gen) << 32;
-  unsigned long long cur = ptx::ld_relaxed_gpu(c);
+  unsigned long long cur =
+      tag | static_cast<uint32_t>(expect > 0 ? expect - 1 : 0);
   for (int i = 0; i < kMaxArrivalTries; ++i) {
     const uint32_t n =
         (cur >> 32) == p.gen ? static_cast<uint32_t>(cur) : 0u;
-    const unsigned long long seen =
-        ptx::atom_cas_acq_rel_gpu(c, cur, tag | (n + 1u));
+    const unsigned long long want = tag | (n + 1u);
+    const unsigned long long seen = ptx::atom_cas_acq_rel_gpu(c, cur, want);
     if (seen == cur) return n;
     cur = seen;
   }
@@ -721,8 +729,6 @@ __device__ __forceinline__ uint32_t arrive_unit(const DecodeParams& p, int u) {
   return 0xffffffffu;
 }
 
-// Shared memory of plan_block.  b0, L0, pref0 and found must be zero, and
-// visible to the whole block, before the call.
 // Warms L2 with the lines of seq_lens (read first after the wait for the
 // previous kernel; an L2 prefetch returns nothing to the thread, so it may be
 // issued before that wait).  Threads 0..31 of the block.
@@ -873,6 +879,38 @@ __device__ __forceinline__ void plan_block(const DecodeParams& p, int HU,
   }
 }
 
+// Warms L2 with the query rows of unit (b, kvh, hc): one bulk prefetch of
+// the unit's contiguous rows of q [B, Hq, T, D] (16-bit).
+template <int D>
+__device__ __forceinline__ void prefetch_unit_q(const DecodeParams& p, int b,
+                                                int kvh, int hc) {
+  const int rows = min(p.R, p.GR - hc * p.R);
+  if (rows <= 0) return;
+  const size_t row0 =
+      (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * p.G) * p.T +
+      static_cast<size_t>(hc) * p.R;
+  ptx::bulk_prefetch_l2(static_cast<const uint16_t*>(p.q) + row0 * D,
+                        static_cast<uint32_t>(rows * D * 2));
+}
+
+// Warms L2 with the query rows of the units that start inside this block's
+// tile range [t0, t1) after its first one (at most kQPrefetchUnits), so that
+// a change of unit late in the range does not wait for them in HBM.  One
+// thread; w is the walk position of tile t0.
+template <int D, int TT>
+__device__ __forceinline__ void prefetch_range_q(const DecodeParams& p, int HU,
+                                                 TileWalkT<TT> w, long long t0,
+                                                 long long t1) {
+  long long g = t0;
+  for (int k = 0; k < kQPrefetchUnits; ++k) {
+    g += w.nt - w.ti;  // the next unit's first tile
+    if (g >= t1) return;
+    w.ti = w.nt - 1;
+    w.next(p, HU);
+    prefetch_unit_q<D>(p, w.b, w.j / p.NHC, w.j % p.NHC);
+  }
+}
+
 // Warms L2 with this block's first tiles, guessing that every sequence fills
 // its cache (exact for uniform lengths; a wrong guess only costs bandwidth).
 // Uses kernel parameters only, so it may run before the previous kernel in
@@ -883,10 +921,11 @@ __device__ __forceinline__ void plan_block(const DecodeParams& p, int HU,
 template <int KV, int D, int HB, int TT = kTileTokens>
 __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
                                                      const CUtensorMap* map_v,
-                                                     int B, int Hkv, int NHC,
-                                                     int Smax, int p_align,
+                                                     const DecodeParams& p,
                                                      int lane) {
   using C = Cfg<KV, D, HB>;
+  const int B = p.B, Hkv = p.Hkv, NHC = p.NHC, Smax = p.Smax;
+  const int p_align = p.p_align;
   // the same bytes whatever the tile length: kPrefetchTiles 64-token tiles
   constexpr int kTiles = kPrefetchTiles * kTileTokens / TT;
   const unsigned nt = (static_cast<unsigned>(Smax) + TT - 1) / TT;
@@ -909,6 +948,11 @@ __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
     const int plane = static_cast<int>(bq) * Hkv +
                       static_cast<int>(rem / nt) / NHC;
     const int tok = static_cast<int>(rem % nt) * TT;
+    if (lane == 0) {
+      // the query rows of the first unit
+      const int jj = static_cast<int>(rem / nt);
+      prefetch_unit_q<D>(p, static_cast<int>(bq), jj / NHC, jj % NHC);
+    }
 #pragma unroll
     for (int th = 0; th < TT / kTileTokens; ++th)
 #pragma unroll
@@ -963,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_npend;
   __shared__ int s_pend_u[2], s_pend_b[2], s_pend_j[2], s_pend_cf[2],
       s_pend_cl[2], s_pend_last[2];
-  __shared__ uint32_t s_pend_t[2];
+  __shared__ volatile uint32_t s_pend_t[2];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -977,8 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tensormap(&map_v);
     }
     if constexpr (!PAGED)
-      prefetch_first_tiles<KV, D, HB>(&map_k, &map_v, p.B, p.Hkv, p.NHC,
-                                      p.Smax, p.p_align, lane);
+      prefetch_first_tiles<KV, D, HB>(&map_k, &map_v, p, lane);
   }
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -1083,6 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     // ================================= merge =================================
     const int mt = tid - 32;  // 0 .. kMergeThreads-1
+    if (mt == 0 && t0 < t1) prefetch_range_q<D, kTileTokens>(p, HU, w0, t0, t1);
     // Sequences with no valid token: all-zero output rows.
     for (int b = cta; b < p.B; b += gridDim.x) {
       if (clamp_len(__ldg(p.seq_lens + b), p.Smax) != 0) continue;
@@ -1116,11 +1160,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           mt, dmp_o, dmp_m, dmp_l, s_rowlse, p, u, bq, j, whole, cta);
       // A partial also counts this block's arrival (acquire-release add: the
       // merge warps' partial stores are ordered before it by their barrier);
-      // the ticket is kept for the combine after the block's last unit.
+      // the ticket is kept for the combine after the block's last unit.  The
+      // dump area is handed back first (merge_unit's last barrier: no merge
+      // thread reads it any more), so that the consumers' next dump does not
+      // wait for the arrival's release of the partial stores.
       if (mt == 0) {
+        // the slot first (its ticket marked pending), then the dump area,
+        // then the arrival and its ticket
+        int k = -1;
         if (!whole && s_npend < 2) {
-          const int k = s_npend;
-          s_pend_t[k] = arrive_unit(p, u);
+          k = s_npend;
+          s_pend_t[k] = kTicketPending;
           s_pend_u[k] = u;
           s_pend_b[k] = bq;
           s_pend_j[k] = j;
@@ -1128,7 +1178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_pend_cl[k] = c_last;
           s_npend = k + 1;
         }
-        ptx::mbar_arrive(dump_empty);  // the dump area is free again
+        ptx::mbar_arrive(dump_empty);
+        if (k >= 0) {
+          const uint32_t tk = arrive_unit(p, u, c_last - c_first + 1);
+          __threadfence_block();
+          s_pend_t[k] = tk;
+        }
       }
     }
   }
@@ -1726,12 +1781,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     const int u = s_du, c_first = s_dcf, c_last = s_dcl;
     const bool whole = (c_first == c_last);
+    const int expect = c_last - c_first + 1;  // blocks of a split unit
+    // Have the unit's other blocks all arrived?  Read (with acquire) while
+    // the merge runs.  If so this block is the last one: it combines at once,
+    // with no arrival of its own and so without waiting for its partial
+    // stores to be released (its own threads see them through the barrier).
+    unsigned long long seen = 0ull;
+    if (ct == 0 && !whole) seen = ptx::ld_acquire_gpu(p.counters + u);
     merge_unit<KV, QBF16, D, HB, kConsumerThreads, 1>(
         ct, dmp_o, dmp_m, dmp_l, s_rowlse, p, u, s_db, s_dj, whole, cta);
     if (ct == 0) {
       if (!whole && s_npend < 2) {
         const int k = s_npend;
-        s_pend_t[k] = arrive_unit(p, u);
+        const unsigned long long all_others =
+            (static_cast<unsigned long long>(p.gen) << 32) |
+            static_cast<uint32_t>(expect - 1);
+        s_pend_t[k] = seen == all_others ? static_cast<uint32_t>(expect - 1)
+                                         : arrive_unit(p, u, expect);
         s_pend_u[k] = u;
         s_pend_b[k] = s_db;
         s_pend_j[k] = s_dj;
@@ -1739,6 +1805,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_pend_cl[k] = c_last;
         s_npend = k + 1;
       }
+      // A merge warp's ticket may still be on its way (its arrival runs
+      // after it handed the dump area back): wait for it (bounded).
+      const uint64_t t_start = ptx::globaltimer_ns();
+      for (int i = 0; i < s_npend; ++i)
+        while (s_pend_t[i] == kTicketPending) {
+          if (ptx::globaltimer_ns() - t_start > p.wait_ns) {
+            atomicOr(p.error, kErrWaitTimeout);
+            s_pend_t[i] = 0xffffffffu;  // matches no arrival count
+          }
+        }
+      __threadfence_block();
       // last arrival of a unit: this block combines its partials
       // (the acquire side of both adds: what the other blocks released
       // before their arrivals is visible to this thread, and to the

@@ -215,8 +215,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     // (a paged cache's pages are only known from the block table, which the
     // previous kernel may write)
     if constexpr (!PAGED)
-      prefetch_first_tiles<kKv, D, 4, TT>(&map_k, &map_v, p.B, p.Hkv, p.NHC,
-                                          p.Smax, p.p_align, lane);
+      prefetch_first_tiles<kKv, D, 4, TT>(&map_k, &map_v, p, lane);
   }
   if (tid == 0) {
     for (int s = 0; s < kUmmaStages; ++s) {
@@ -510,6 +509,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     }
   }
 
+  if (st_id == 0 && t0 < t1) prefetch_range_q<D, TT>(p, HU, w0, t0, t1);
   if (t0 < t1) {
     TileWalkT<TT> w = w0;
     long long it = 0;
@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
           ptx::named_bar_sync(kBarSoftmax, kUmmaSoftmaxThreads);
           if (!whole && st_id == 0 && s_npend < 2) {
             const int k = s_npend;
-            s_pend_t[k] = arrive_unit(p, u);
+            s_pend_t[k] = arrive_unit(p, u, cl - cf + 1);
             s_pend_u[k] = u;
             s_pend_b[k] = w.b;
             s_pend_j[k] = w.j;

@@ -129,6 +129,15 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0,
       : "memory");
 }
 
+// Warms L2 with `bytes` bytes from `ptr` (both multiples of 16; no data
+// returned, nothing to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* ptr,
+                                                 uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr),
+               "r"(bytes)
+               : "memory");
+}
+
 // Warms L2 with the 128-byte line holding `ptr` (no data returned).
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
@@ -273,10 +282,12 @@ __device__ __forceinline__ unsigned long long atom_cas_acq_rel_gpu(
   return old;
 }
 
-__device__ __forceinline__ unsigned long long ld_relaxed_gpu(
+// Acquire load at GPU scope: later loads of this thread see what other
+// threads released before the value they stored.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(
     const unsigned long long* addr) {
   unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];"
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];"
                : "=l"(v)
                : "l"(addr)
                : "memory");
