@@ -112,29 +112,37 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(workload: str):
+TRAFFIC_SUMMARY = os.path.join("profiles",
+                               "gqa_decode__dram_traffic_all_workloads.md")
+
+
+def profiled_traffic(workload: str, algo_bytes: int = 0):
     """DRAM bytes (read + write) per launch of the decode kernel on this
-    workload, from the ncu summary committed under profiles/, or None when
-    there is none or the kernel sources changed since it was captured."""
-    path = os.path.join(ROOT, "profiles", f"gqa_decode_kernel__{workload}.md")
+    workload, from the ncu summary committed under profiles/ (scaled by this
+    run's algorithmic bytes when they differ from the captured step's), or
+    None when there is none or the kernel sources changed since it was
+    captured."""
+    path = os.path.join(ROOT, TRAFFIC_SUMMARY)
     try:
         with open(path) as f:
             text = f.read()
     except OSError:
         return None
-    vals = {}
+    sha, found = None, None
     for line in text.splitlines():
         line = line.strip().lstrip("-").strip()
-        if ":" in line and line.startswith(("traffic_bytes_per_launch",
-                                            "kernel_sources_sha256")):
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_sources_sha256") != kernel_sources_sha256():
+        if line.startswith("kernel_sources_sha256:"):
+            sha = line.split(":", 1)[1].strip().strip("`")
+        elif line.startswith(f"traffic_bytes_per_launch {workload}:"):
+            parts = [x for x in line.split("`") if x.strip().isdigit()]
+            if len(parts) >= 2:
+                found = (int(parts[0]), int(parts[1]))
+    if sha != kernel_sources_sha256() or found is None:
         return None
-    try:
-        return int(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    traffic, algo = found
+    if algo_bytes and algo and algo_bytes != algo:
+        return int(round(traffic * algo_bytes / algo))
+    return traffic
 
 
 def load_peaks():
@@ -383,7 +391,7 @@ def measure_config(name, w, dev, stream, flush, warmup, K, peak, peak_kind,
               "L2 flushed before every step: median of 50 launches",
         "kv_gbs": achieved, "frac": achieved / peak, "peak": peak,
         "peak_kind": peak_kind, "algorithmic_bytes_per_step": algo,
-        "traffic": profiled_traffic(name),
+        "traffic": profiled_traffic(name, algo),
         "back_to_back": _dist(b2b), "cold_l2": _dist(cold),
         "launches_per_step": gq.gqa_last_launch_count(),
     }
@@ -522,7 +530,9 @@ def profile_launches(w, name, dev, n: int) -> int:
         step()
     torch.cuda.synchronize()
     err = gq.gqa_device_errors(stream)
-    print(json.dumps({"profile_launches": n, "workload": name,
+    print(json.dumps({"profile_launches": n, "workload": name, "B": w.B,
+                      "algorithmic_bytes_per_step":
+                          w.algorithmic_bytes(inp["seq_lens"].cpu()),
                       "device_errors": err,
                       "launches_per_step": gq.gqa_last_launch_count()}),
           flush=True)
@@ -570,11 +580,19 @@ def main(argv=None):
     ap.add_argument("--num-ctas", type=int, default=0,
                     help="blocks per launch (0: the library's own choice, "
                          "the default; for A/B comparisons of the split)")
+    ap.add_argument("--tune", type=int, default=0,
+                    help="GQA_TUNE_* bits: design choices turned off for "
+                         "A/B comparisons (1 no L2 warm-up, 2 no clusters, "
+                         "4 no narrow rows); 0 (default) keeps all")
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="profiling mode: build the workload's inputs, "
                          "launch exactly this many decode steps, check the "
                          "error flags and exit (no timing, no other "
                          "kernels after the inputs are drawn)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling mode only: the workload with this many "
+                         "sequences instead of its own B (a smaller capture "
+                         "of the same shape; per-sequence figures scale)")
     a = ap.parse_args(argv)
 
     from grouped_query_attention_11_b300.workloads import (HEADLINE,
@@ -637,12 +655,18 @@ def main(argv=None):
     gq.lib()
     gq.gqa_set_num_ctas(a.num_ctas)
     gq.gqa_set_kernel_path(a.kernel_path)
+    gq.gqa_set_tuning(a.tune)
+    if a.tune:
+        cfg["tune"] = a.tune
     if a.num_ctas:
         cfg["num_ctas"] = a.num_ctas
     cfg["kernel_path"] = ("automatic", "warp-level mma",
                           "tensor core where it applies")[a.kernel_path]
 
     if a.profile_launches > 0:
+        if a.batch > 0:
+            import dataclasses
+            w = dataclasses.replace(w, B=a.batch)
         return profile_launches(w, name, dev, a.profile_launches)
 
     inp = make_inputs(w, pad="zero", seed=w.seed + rank)
@@ -737,7 +761,7 @@ def main(argv=None):
         return 0
 
     achieved = algo_bytes / (us * 1e-6) / 1e9
-    traffic = profiled_traffic(name)
+    traffic = profiled_traffic(name, algo_bytes)
     clocks = sampler.summary() if sampler else None
     if clocks is not None:
         clocks["window"] = "warm-up, settle and timed region"

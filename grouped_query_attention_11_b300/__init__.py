@@ -22,6 +22,7 @@ its names:
 * :func:`gqa_kv_bytes_per_token`, :func:`gqa_status_string`,
   :func:`gqa_device_errors`, :func:`gqa_set_num_ctas`,
   :func:`gqa_set_wait_limit_ns`, :func:`gqa_set_kernel_path`,
+  :func:`gqa_set_tuning`,
   :func:`gqa_last_launch_count`.
 """
 from __future__ import annotations
@@ -59,6 +60,7 @@ SIGNATURES = {
     "gqa_set_num_ctas": (None, [_I32]),
     "gqa_set_wait_limit_ns": (None, [ctypes.c_longlong]),
     "gqa_set_kernel_path": (None, [_I32]),
+    "gqa_set_tuning": (None, [_I32]),
     "gqa_last_launch_count": (_I32, []),
 }
 
@@ -106,6 +108,17 @@ def gqa_set_kernel_path(path: int) -> None:
     """Test / tuning hook: 0 automatic, 1 warp-level mma kernel only, 2
     tensor-core kernel wherever it applies."""
     lib().gqa_set_kernel_path(int(path))
+
+
+GQA_TUNE_NO_L2_WARMUP = 1
+GQA_TUNE_NO_CLUSTER = 2
+GQA_TUNE_NO_NARROW_ROWS = 4
+
+
+def gqa_set_tuning(flags: int) -> None:
+    """Tuning hook: an OR of GQA_TUNE_* bits turns single design choices off
+    (A/B measurements); 0 keeps all of them."""
+    lib().gqa_set_tuning(int(flags))
 
 
 def gqa_set_wait_limit_ns(ns: int) -> None:

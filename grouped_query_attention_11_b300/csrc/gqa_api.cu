@@ -166,8 +166,9 @@ Variant pick_d(int D, int hb) {
 
 // Paged caches are instantiated for the 16-bit element types.  rows: query
 // rows per unit (R).
-Variant pick(int kv, bool q_bf16, int D, int hb, int rows, bool paged = false) {
-  if (is_fp8(kv) && rows <= 8)
+Variant pick(int kv, bool q_bf16, int D, int hb, int rows, bool paged = false,
+             bool narrow = true) {
+  if (is_fp8(kv) && rows <= 8 && narrow)
     return kv == kKvE5M2 ? pick_nr<kKvE5M2>(q_bf16, D)
                          : pick_nr<kKvE4M3>(q_bf16, D);
   if (paged)
@@ -217,10 +218,16 @@ std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 int g_num_ctas_override = 0;
 uint64_t g_wait_ns = kWaitLimitNs;
 // Kernel choice: 0 automatic (the tensor-core kernel for units of more than
-// 16 query rows with a 16-bit cache, head_dim 128, contiguous), 1 the
+// kUmmaMinRows query rows with a 16-bit cache and head_dim 128), 1 the
 // warp-level mma kernel everywhere, 2 the tensor-core kernel wherever it
-// applies (also for units of up to 16 rows).
+// applies (also for units of fewer rows).
 int g_kernel_path = 0;
+// Units of more rows than this go to the tensor-core kernel by default.
+// Measured (back-to-back steps): 64-row units (multi-query attention) 22.8
+// us against 32.1 us on the warp-level kernel; 32-row units (the 70B
+// shape's 4-token chunk) 55.2 us against 54.0 us, so they stay there.
+constexpr int kUmmaMinRows = 32;
+int g_tuning = 0;  // GQA_TUNE_* bits: design choices turned off
 thread_local int t_last_launches = 0;
 
 constexpr size_t kHeaderBytes = 256;  // error word(s)
@@ -393,10 +400,12 @@ gqa_status launch(const void* q, const void* k, const void* v,
 
   // the tensor-core kernel: 16-bit caches, head_dim 128
   const bool umma = !is_fp8(kv_kind) && D == kUmmaD &&
-                    (g_kernel_path == 2 || (g_kernel_path == 0 && R > 16));
+                    (g_kernel_path == 2 ||
+                     (g_kernel_path == 0 && R > kUmmaMinRows));
   const int tile_tokens = umma ? kUmmaTileTokens : kTileTokens;
   const int rows_pad = umma ? kUmmaCols : hb * 16;
-  const Variant var = pick(kv_kind, q_bf16, D, hb, R, paged);
+  const Variant var = pick(kv_kind, q_bf16, D, hb, R, paged,
+                           !(g_tuning & GQA_TUNE_NO_NARROW_ROWS));
   const UmmaVariant uvar = umma ? umma_variant(q_bf16, R, paged)
                                 : UmmaVariant{};
   const int elem_bytes = is_fp8(kv_kind) ? 1 : 2;
@@ -435,7 +444,8 @@ gqa_status launch(const void* q, const void* k, const void* v,
   // launch those blocks as thread-block clusters, which merge their states
   // through distributed shared memory, when every cluster fits at once.
   int cluster = 0;
-  if (umma && p_align > units && p_align % units == 0) {
+  if (umma && p_align > units && p_align % units == 0 &&
+      !(g_tuning & GQA_TUNE_NO_CLUSTER)) {
     const int k = static_cast<int>(p_align / units);
     if ((k == 2 || k == 4) &&
         max_clusters(dev, reinterpret_cast<const void*>(uvar.fn), uvar.smem,
@@ -480,6 +490,7 @@ gqa_status launch(const void* q, const void* k, const void* v,
   p.R = R;
   p.p_align = p_align;
   p.cluster = cluster;
+  p.tune = g_tuning;
   p.block_table = block_table;
   p.max_pages = paged ? Smax / page_size : 0;
   p.page_size = page_size;
@@ -733,6 +744,12 @@ gqa_status gqa_device_errors(void* stream_ptr, uint32_t* flags) {
 void gqa_set_kernel_path(int path) {
   std::lock_guard<std::mutex> lock(gqa::g_mu);
   gqa::g_kernel_path = (path == 1 || path == 2) ? path : 0;
+}
+
+void gqa_set_tuning(int flags) {
+  std::lock_guard<std::mutex> lock(gqa::g_mu);
+  gqa::g_tuning = flags & (GQA_TUNE_NO_L2_WARMUP | GQA_TUNE_NO_CLUSTER |
+                           GQA_TUNE_NO_NARROW_ROWS);
 }
 
 void gqa_set_wait_limit_ns(long long ns) {

@@ -162,6 +162,9 @@ struct DecodeParams {
   // their states are then merged through distributed shared memory.  0 or
   // 1: no cluster launch.
   int cluster;
+  // Design choices turned off for A/B measurements (bit 0: no L2 warm-up
+  // before the dependent-launch wait).
+  int tune;
 };
 
 // ------------------------------------------------------------ compile-time
@@ -1021,7 +1024,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tensormap(&map_v);
     }
     if constexpr (!PAGED)
-      prefetch_first_tiles<KV, D, HB>(&map_k, &map_v, p, lane);
+      if (!(p.tune & 1))
+        prefetch_first_tiles<KV, D, HB>(&map_k, &map_v, p, lane);
   }
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {

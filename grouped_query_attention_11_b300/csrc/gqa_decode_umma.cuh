@@ -1,5 +1,5 @@
 // gqa_decode_umma.cuh — the GQA decode step on the fifth-generation tensor
-// core (tcgen05) for units with many query rows: 17 to 64 query rows share
+// core (tcgen05) for units with many query rows: up to 64 query rows share
 // one KV head (multi-query attention, wide groups, multi-token causal chunks).
 //
 // What one launch computes: the same as gqa_decode_kernel (softmax(scale *
@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     // (a paged cache's pages are only known from the block table, which the
     // previous kernel may write)
     if constexpr (!PAGED)
-      prefetch_first_tiles<kKv, D, 4, TT>(&map_k, &map_v, p, lane);
+      if (!(p.tune & 1))
+        prefetch_first_tiles<kKv, D, 4, TT>(&map_k, &map_v, p, lane);
   }
   if (tid == 0) {
     for (int s = 0; s < kUmmaStages; ++s) {

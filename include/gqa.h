@@ -279,14 +279,36 @@ gqa_status gqa_device_errors(void* stream, uint32_t* flags);
  * gqa_set_kernel_path — test and tuning hook: which kernel the decode calls
  * launch (process-wide; host only).  0 (the default): the tensor-core kernel
  * (fifth-generation tensor core, accumulators in tensor memory) for units of
- * more than 16 query rows per KV head with a 16-bit cache, head_dim 128 and
- * a contiguous cache (multi-query attention, wide groups, multi-token
- * chunks), the warp-level mma kernel otherwise.  1: the warp-level kernel
- * everywhere.  2: the tensor-core kernel wherever it applies, units of up to
- * 16 rows included.  The result is the same within the stated tolerance
+ * more than 32 query rows per KV head with a 16-bit cache and head_dim 128
+ * (multi-query attention, wide groups, multi-token chunks of wide groups;
+ * contiguous or paged), the warp-level mma kernel otherwise.  1: the
+ * warp-level kernel everywhere.  2: the tensor-core kernel wherever it
+ * applies, units of up to 32 rows included.  The result is the same within the stated tolerance
  * (fp32 accumulation both ways); other values count as 0.
  */
 void gqa_set_kernel_path(int path);
+
+/*
+ * gqa_set_tuning — test and tuning hook (process-wide; host only): turns
+ * single design choices of the decode calls off, for A/B measurements.  An
+ * OR of GQA_TUNE_* bits; 0 (the default) keeps every choice.
+ *   GQA_TUNE_NO_L2_WARMUP    no L2 prefetch of a block's first tiles and
+ *                            first query rows before its wait for the
+ *                            previous kernel in the stream
+ *   GQA_TUNE_NO_CLUSTER      the tensor-core kernel never launches thread-
+ *                            block clusters (units split between blocks
+ *                            always merge through global memory)
+ *   GQA_TUNE_NO_NARROW_ROWS  8-bit caches with at most 8 query rows per unit
+ *                            take the 16-row operand path
+ * The result is the same within the stated tolerance; unknown bits are
+ * ignored.
+ */
+enum {
+  GQA_TUNE_NO_L2_WARMUP = 1,
+  GQA_TUNE_NO_CLUSTER = 2,
+  GQA_TUNE_NO_NARROW_ROWS = 4
+};
+void gqa_set_tuning(int flags);
 
 /*
  * gqa_set_wait_limit_ns — test hook: the time limit of every pipeline wait in

@@ -33,9 +33,10 @@ def _fake_root(tmp_path, traffic, sha):
                                  "csrc", name), csrc / name)
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "gqa_decode_kernel__w.md").write_text(
+    (tmp_path / bench.TRAFFIC_SUMMARY).write_text(
         "# summary\n\n"
-        f"- traffic_bytes_per_launch: `{traffic}`\n"
+        f"- traffic_bytes_per_launch w: `{traffic}` for `1000` algorithmic "
+        "bytes\n"
         f"- kernel_sources_sha256: `{sha}`\n")
     return str(tmp_path)
 
@@ -45,6 +46,9 @@ def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", _fake_root(tmp_path, 12345, sha))
     assert bench.kernel_sources_sha256() == sha
     assert bench.profiled_traffic("w") == 12345
+    assert bench.profiled_traffic("w", 1000) == 12345
+    # another draw of the workload: scaled by its algorithmic bytes
+    assert bench.profiled_traffic("w", 2000) == 24690
     assert bench.profiled_traffic("missing") is None
     # a comment added to a kernel source keeps the summary valid ...
     src = tmp_path / "grouped_query_attention_11_b300" / "csrc" / \

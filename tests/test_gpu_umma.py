@@ -1,9 +1,10 @@
 """GPU parity of the tensor-core (tcgen05) decode kernel with the fp64 oracle.
 
-The kernel serves units of 17 to 64 query rows per KV head (multi-query
-attention, wide groups, multi-token causal chunks) with a 16-bit cache and
-head_dim 128; gqa_set_kernel_path(2) also sends units of up to 16 rows to it,
-and gqa_set_kernel_path(1) sends everything to the warp-level mma kernel.
+The kernel serves units of 33 to 64 query rows per KV head (multi-query
+attention, wide groups, multi-token causal chunks of wide groups) with a
+16-bit cache and head_dim 128 by default; gqa_set_kernel_path(2) also sends
+units of up to 32 rows to it (its 32-column variant), and
+gqa_set_kernel_path(1) sends everything to the warp-level mma kernel.
 Each case runs under all three settings against the same oracle output, on
 NaN-padded caches, with sequences that end inside a tile, empty sequences,
 units split between blocks and row chunks of a KV head (more than 64 rows)."""
@@ -43,7 +44,7 @@ CASES = [
     ("whole_tiles", 2, 64, 2, 256, "bf16", ("uniform",), 1),
     ("smax_not_tile_multiple", 2, 64, 1, 100, "bf16", ("uniform",), 1),
     ("many_sequences", 300, 32, 1, 90, "bf16", ("ragged", 0, 90), 1),
-    # units of at most 16 rows: the tensor-core kernel only under path 2
+    # units of at most 32 rows: the tensor-core kernel only under path 2
     ("g8_small", 2, 64, 8, 515, "bf16", ("list", 515, 200), 1),
     ("g4_f16_small", 3, 32, 8, 300, "f16", ("list", 300, 1, 129), 1),
     ("mha_g1", 2, 8, 8, 190, "bf16", ("list", 190, 77), 1),
