@@ -592,7 +592,9 @@ __device__ __forceinline__ void merge_unit(int t, const uint8_t* dmp_o,
     float acc[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[x] = 0.f;
-#pragma unroll 1
+    // the consumer threads (registers to spare after their tile loop) keep
+    // every warp's loads in flight together; the merge warps, one at a time
+#pragma unroll (kNT >= 256 ? 8 : 1)
     for (int k = 0; k < kW; ++k) {
       const int wk = warp_of(hbk, k);
       const float wt = dmp_m[wk * 16 + rr];
