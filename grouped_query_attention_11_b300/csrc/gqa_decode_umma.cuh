@@ -85,7 +85,7 @@ constexpr int kUmmaQOff = kUmmaStages * kUmmaStageBytes;
 constexpr int kUmmaRedOff = kUmmaQOff + 2 * kUmmaQBytes;    // [4][64] fp32
 constexpr int kUmmaVecOff = kUmmaRedOff + 4 * 64 * 4;       // m, alpha [64]
 constexpr int kUmmaBarOff = kUmmaVecOff + 2 * 64 * 4;
-constexpr int kUmmaBars = 16;
+constexpr int kUmmaBars = 17;
 constexpr int kUmmaSmemBytes = 1024 + kUmmaBarOff + kUmmaBars * 8 + 16;
 static_assert(kUmmaSmemBytes + 256 <= 232448,
               "shared memory of the tensor-core kernel exceeds the limit");
@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   uint64_t* qempty = qfull + 2;            // [2]  unit's last S done -> producer
   uint64_t* sfull = qempty + 2;            // [2]  S ready -> softmax
   uint64_t* pfull = sfull + 2;             // [2]  P written -> MMA (8 warps)
-  uint64_t* oready = pfull + 2;            // PV of a tile done -> softmax
-  uint64_t* mma_done = oready + 1;         // every product done (teardown)
+  uint64_t* oready = pfull + 2;            // [2]  PV of tile i done (i & 1)
+  uint64_t* mma_done = oready + 2;         // every product done (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kUmmaBars);
 
   __shared__ PlanSmem<kUmmaThreads> s_plan;
@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
       ptx::mbar_init(&sfull[i], 1);
       ptx::mbar_init(&pfull[i], kUmmaSoftmaxThreads / 32);
     }
-    ptx::mbar_init(oready, 1);
+    ptx::mbar_init(&oready[0], 1);
+    ptx::mbar_init(&oready[1], 1);
     ptx::mbar_init(mma_done, 1);
     ptx::fence_barrier_init();
     s_abort = 0;
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
           umma_f16_ts(tmem + kTmL, tmem + kTmOnes + 8 * k, pd, kIdescL, acc);
         }
         ptx::umma_commit(&empty[pv_stage]);
-        ptx::umma_commit(oready);
+        ptx::umma_commit(&oready[pv_it & 1]);
         pv_pending = false;
       };
       for (long long g = t0; g < t1 && !aborted; ++g, ++it) {
@@ -526,11 +527,15 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         aborted = true;
       }
     };
-    // PV(i) (block tile index) has completed.  Called for every tile in
-    // order (never more than one phase behind, as parity waits require).
+    // PV(i) (block tile index) has completed.  The PV products alternate
+    // between two barriers; each barrier's phases are consumed in order and
+    // never more than one behind, as parity waits require: PV(i + 2) cannot
+    // complete before this thread publishes P(i + 2), and by then PV(i) has
+    // been waited for.
     auto wait_pv = [&](long long i) {
       while (pv_waited <= i) {
-        wait_ok(oready, static_cast<uint32_t>(pv_waited & 1));
+        wait_ok(&oready[pv_waited & 1],
+                static_cast<uint32_t>((pv_waited >> 1) & 1));
         ++pv_waited;
       }
     };
@@ -627,7 +632,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
         load_scores(x);
       }
-      if (it >= 1) wait_pv(it - 1);
+      // The probabilities do not wait for the previous tile's PV (it reads
+      // another stage): only PV(it - 2), on the barrier PV(it) completes.
+      if (it >= 2) wait_pv(it - 2);
 
       // ---- probabilities into P^T (this token's row of the stage's K half;
       // the warpgroup's NH rows = NH * 2 bytes)
