@@ -1207,7 +1207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t qf[C::kQSteps][4];
   float o[C::kOAcc][4];
   float m[2], l[2];
-  float s_mult = 0.f, o_mult = 1.f;
+  float s_mult = 0.f;
   bool fresh = true;
   bool aborted = false;  // this warp gave up on a wait: skip further waits
   // Last key each of this thread's two rows may see: new token i of a chunk
@@ -1220,7 +1220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // This thread's two fragment rows within its head block, and their query
   // rows for unit (kvh, hc) of sequence b.
   const int row0 = hb * 16 + r, row1 = row0 + 8;
+  // 8-bit caches: the unit's K scale, loaded with its query rows (it is
+  // needed at the unit's first tile, where a load's latency would stall)
+  float k_scale_next = 1.f;
   auto issue_q = [&](int b, int kvh, int hc) {
+    if constexpr (kFp8) k_scale_next = __ldg(p.k_scale + b * p.Hkv + kvh);
     const bool ok0 = row0 < p.R && hc * p.R + row0 < p.GR;
     const bool ok1 = row1 < p.R && hc * p.R + row1 < p.GR;
     const size_t r0 =
@@ -1237,18 +1241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   int par = 0;       // (g - t0) % kGroups: the group that computes tile g
   uint32_t dph = 0;  // parity of this block's unit epilogues so far
   for (long long g = t0; g < t1; ++g) {
-    const int kvh = w.j / p.NHC;
     if (fresh) {
       // ---- new unit: softmax state and multipliers (q already issued) ----
       fresh = false;
       if constexpr (!kFp8) {
         s_mult = p.scale_log2;
-        o_mult = 1.f;
       } else {
         const int e = fp8_finish_q<QBF16, D>(qf);
-        const int sidx = w.b * p.Hkv + kvh;
-        s_mult = p.scale_log2 * __ldg(p.k_scale + sidx) * ldexpf(1.f, -e);
-        o_mult = __ldg(p.v_scale + sidx);
+        s_mult = p.scale_log2 * k_scale_next * ldexpf(1.f, -e);
       }
 #pragma unroll
       for (int n = 0; n < C::kOAcc; ++n)
