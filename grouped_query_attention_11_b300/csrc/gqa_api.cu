@@ -467,6 +467,8 @@ gqa_status launch(const void* q, const void* k, const void* v,
 
   DecodeParams p = {};
   p.q = q;
+  p.kc = paged ? nullptr : k;
+  p.vc = paged ? nullptr : v;
   p.out = out;
   p.seq_lens = seq_lens;
   p.k_scale = k_scale;
@@ -615,6 +617,8 @@ gqa_status launch_static(const void* q, const void* k, const void* v,
 
   DecodeParams p = {};
   p.q = q;
+  p.kc = k;
+  p.vc = v;
   p.out = out;
   p.seq_lens = seq_lens;
   p.k_scale = nullptr;

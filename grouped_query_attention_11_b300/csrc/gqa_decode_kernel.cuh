@@ -129,6 +129,10 @@ enum ErrorBits : uint32_t {
 
 struct DecodeParams {
   const void* q;            // [B, Hq, D] f16 / bf16
+  // the caches' base addresses (contiguous caches only; they are read
+  // through the tensor maps, these only warm L2)
+  const void* kc;
+  const void* vc;
   void* out;                // [B, Hq, D] same dtype as q
   const int32_t* seq_lens;  // [B]
   const float* k_scale;     // [B, Hkv] (E4M3 only)
@@ -923,7 +927,7 @@ __device__ __forceinline__ void prefetch_range_q(const DecodeParams& p, int HU,
 // divide only: a 64-bit or IEEE division here compiles to a called routine
 // that costs the whole kernel registers.  The start tile only needs to be
 // close; problems with more than 2^31 tiles skip the prefetch.
-template <int KV, int D, int HB, int TT = kTileTokens>
+template <int KV, int D, int HB, int TT = kTileTokens, bool BULK = false>
 __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
                                                      const CUtensorMap* map_v,
                                                      const DecodeParams& p,
@@ -945,6 +949,35 @@ __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* map_k,
   // approximate start tile (no IEEE division: its slow path is a call)
   unsigned x0 = static_cast<unsigned>(
       __fdividef(static_cast<float>(ng), static_cast<float>(pg)) * blockIdx.x);
+  if (BULK && NHC == 1 && p.kc != nullptr) {
+    // one KV head per unit: the guessed range is contiguous in each cache
+    // ([B*Hkv][Smax][D], plane x / nt): one bulk prefetch of K and one of V
+    // instead of one per box and tile, which the TMA unit issues one at a
+    // time at the block's start (measured: faster for the tensor-core
+    // kernel's multi-query steps, slower for the warp-level kernel's)
+    if (lane == 0 && x0 < ng) {
+      const unsigned plane = x0 / nt;
+      const unsigned long long row = static_cast<unsigned long long>(D) *
+                                     C::kElemBytes;
+      const unsigned long long start =
+          (static_cast<unsigned long long>(plane) * Smax + (x0 % nt) * TT) *
+          row;
+      const unsigned long long total =
+          static_cast<unsigned long long>(B) * Hkv * Smax * row;
+      unsigned long long len =
+          static_cast<unsigned long long>(kPrefetchTiles) * kTileTokens * row;
+      if (start < total) {
+        if (len > total - start) len = total - start;
+        ptx::bulk_prefetch_l2(static_cast<const uint8_t*>(p.kc) + start,
+                              static_cast<uint32_t>(len));
+        ptx::bulk_prefetch_l2(static_cast<const uint8_t*>(p.vc) + start,
+                              static_cast<uint32_t>(len));
+      }
+      prefetch_unit_q<D>(p, static_cast<int>(plane) / Hkv,
+                         static_cast<int>(plane) % Hkv, 0);
+    }
+    return;
+  }
   // lane k prefetches tile k of the range (one warp, no divergence in the
   // arithmetic)
   x0 += lane;

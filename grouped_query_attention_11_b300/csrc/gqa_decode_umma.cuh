@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     // previous kernel may write)
     if constexpr (!PAGED)
       if (!(p.tune & 1))
-        prefetch_first_tiles<kKv, D, 4, TT>(&map_k, &map_v, p, lane);
+        prefetch_first_tiles<kKv, D, 4, TT, true>(&map_k, &map_v, p, lane);
   }
   if (tid == 0) {
     for (int s = 0; s < kUmmaStages; ++s) {
