@@ -25,8 +25,9 @@
 //    consumers (224) for their mma fragments, accumulators and query rows.
 //  * Launch overlap.  Launched as a programmatic dependent: before
 //    griddepcontrol.wait a block only initialises barriers and asks L2 for
-//    its first tiles (cp.async.bulk.prefetch.tensor), which overlaps the
-//    previous kernel's last blocks; every global read comes after the wait.
+//    seq_lens, its first tiles (cp.async.bulk.prefetch.tensor) and its first
+//    unit's query rows, which overlaps the previous kernel's last blocks;
+//    every global read comes after the wait.
 //  * KV stream.  The producer warp issues TMA tensor loads (128-byte
 //    swizzle, L2 evict-first) of the K and V tiles into a multi-stage shared
 //    memory ring guarded by mbarriers.  Each KV byte is read from HBM once and
@@ -58,7 +59,9 @@
 //    otherwise each block writes a normalised partial (O, log2-sum-exp) and
 //    bumps a per-unit counter; the block that arrives last merges all
 //    partials of the unit (after its own last unit) and writes the output,
-//    then resets the counter.  No block ever waits on another block.  The
+//    then resets the counter.  A block that finds, while it merges its last
+//    unit, that the unit's other blocks have all arrived combines at once
+//    without an arrival of its own.  No block ever waits on another block.  The
 //    counters carry the launch's generation, so a count that a launch left
 //    behind (because one of its waits gave up) is never taken for this one's.
 //  * Paged cache (PAGED).  Only the producer changes: each tile's page comes
