@@ -23,7 +23,7 @@ its names:
   :func:`gqa_device_errors`, :func:`gqa_set_num_ctas`,
   :func:`gqa_set_wait_limit_ns`, :func:`gqa_set_kernel_path`,
   :func:`gqa_set_tuning`,
-  :func:`gqa_last_launch_count`.
+  :func:`gqa_last_launch_count`, :func:`gqa_release_stream`.
 """
 from __future__ import annotations
 
@@ -62,6 +62,7 @@ SIGNATURES = {
     "gqa_set_kernel_path": (None, [_I32]),
     "gqa_set_tuning": (None, [_I32]),
     "gqa_last_launch_count": (_I32, []),
+    "gqa_release_stream": (_I32, [ctypes.c_void_p]),
 }
 
 _lib = None
@@ -125,6 +126,14 @@ def gqa_set_wait_limit_ns(ns: int) -> None:
     """Test hook: time limit of the kernels' pipeline waits (0: give up at the
     first wait that is not already complete; negative: the default)."""
     lib().gqa_set_wait_limit_ns(int(ns))
+
+
+def gqa_release_stream(stream=None) -> None:
+    """Frees the library's scratch for (the current device, stream); a later
+    call on the stream allocates it again."""
+    st = lib().gqa_release_stream(_stream_handle(stream))
+    if st != GQA_OK:
+        raise GQAError(st, "gqa_release_stream")
 
 
 def gqa_last_launch_count() -> int:

@@ -901,4 +901,21 @@ gqa_status gqa_decode_static(const void* q, const void* k_cache,
 
 int gqa_last_launch_count(void) { return gqa::t_last_launches; }
 
+gqa_status gqa_release_stream(void* stream_ptr) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  std::lock_guard<std::mutex> lock(gqa::g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  auto it = gqa::g_scratch.find({dev, stream});
+  if (it == gqa::g_scratch.end()) return GQA_OK;
+  gqa::Scratch& s = it->second;
+  gqa_status st = GQA_OK;
+  if (s.ctl && cudaFreeAsync(s.ctl, stream) != cudaSuccess) st = GQA_ERR_CUDA;
+  if (s.part && cudaFreeAsync(s.part, stream) != cudaSuccess)
+    st = GQA_ERR_CUDA;
+  gqa::g_scratch.erase(it);
+  if (st != GQA_OK) (void)cudaGetLastError();
+  return st;
+}
+
 }  // extern "C"

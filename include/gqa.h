@@ -45,8 +45,9 @@
  * The library keeps a small scratch buffer per (device, stream) for the
  * split-sequence partial results; it is allocated on the first call that needs
  * it (stream-ordered, from the device's default memory pool) and kept for
- * later calls.  Calls on one stream may follow each other freely; calls that
- * share a stream must not run concurrently from several host threads.
+ * later calls (gqa_release_stream frees it).  Calls on one stream may follow
+ * each other freely; calls that share a stream must not run concurrently
+ * from several host threads.
  *
  * Errors.  Argument checks run on the host before anything is launched and
  * return GQA_ERR_INVALID_ARG or GQA_ERR_UNSUPPORTED without touching the GPU.
@@ -330,6 +331,19 @@ void gqa_set_wait_limit_ns(long long ns);
  * only.
  */
 void gqa_set_num_ctas(int num_ctas);
+
+/*
+ * gqa_release_stream — frees the scratch the library keeps for (the current
+ * device, `stream`): stream-ordered frees enqueued on `stream`, after the
+ * work already on it.  Call it before destroying a stream the library used
+ * (the scratch is keyed by the stream handle, which a later stream may
+ * reuse), or to return the memory; a later call on the stream allocates it
+ * again.  The stream's pending fault flags (gqa_device_errors) are dropped
+ * with it.  Returns GQA_OK also when the library holds nothing for the
+ * stream, GQA_ERR_CUDA if a free cannot be enqueued.  Host only; must not
+ * run concurrently with a compute call on the same stream.
+ */
+gqa_status gqa_release_stream(void* stream);
 
 /*
  * gqa_last_launch_count — number of kernels the most recent compute call made
