@@ -4,6 +4,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-cpu-baseline]
                     [--no-per-config] [--op decode|append]
+                    [--kernel-path 0|1|2] [--num-ctas N] [--tune BITS]
+                    [--profile-launches N [--batch B]]
+
+The last four are diagnostics: A/B arms of single design choices (kernel
+choice, block count, GQA_TUNE_* bits) and a profiling mode that only launches
+N steps (optionally of a smaller batch of the same shape) for ncu.
 
 One step = one gqa_decode call over the whole batch of the workload (default:
 the Llama-2/3-70B-shaped long-context decode, B=8, Hq=64, Hkv=8, D=128,
