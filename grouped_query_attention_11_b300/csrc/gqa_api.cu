@@ -904,6 +904,7 @@ int gqa_last_launch_count(void) { return gqa::t_last_launches; }
 gqa_status gqa_release_stream(void* stream_ptr) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   std::lock_guard<std::mutex> lock(gqa::g_mu);
+  if (gqa::g_scratch.empty()) return GQA_OK;  // nothing held: no CUDA call
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   auto it = gqa::g_scratch.find({dev, stream});

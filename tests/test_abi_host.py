@@ -175,3 +175,27 @@ def test_decode_chunk_rejects_invalid_arguments(L):
     assert lib.gqa_decode_chunk(A, A * 2, A * 3, A * 4, 0.125, A * 5, 2, 8, 2,
                                 2, 64, 96, gq.GQA_BF16, None) == \
         gq.GQA_ERR_UNSUPPORTED
+
+
+def header_enum(prefix):
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return {k: int(v) for k, v in re.findall(
+        rf"\b({prefix}[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+
+
+def test_binding_constants_match_the_header():
+    for prefix in ("GQA_TUNE_", "GQA_ERR_", "GQA_E", "GQA_F16", "GQA_BF16"):
+        for name, value in header_enum(prefix).items():
+            assert getattr(gq, name) == value, name
+    assert set(header_enum("GQA_TUNE_")) == {
+        "GQA_TUNE_NO_L2_WARMUP", "GQA_TUNE_NO_CLUSTER",
+        "GQA_TUNE_NO_NARROW_ROWS"}
+
+
+def test_tuning_and_release_need_no_gpu(L):
+    # host-only settings; releasing a stream the library never used is a
+    # no-op (it touches no device)
+    L.gqa_set_tuning(7)
+    L.gqa_set_tuning(0)
+    assert L.gqa_release_stream(None) == gq.GQA_OK
