@@ -140,3 +140,35 @@ def test_tensor_core_kernel_launched():
     gq.decode_inputs(dev)
     assert gq.gqa_last_launch_count() == 1
     assert gq.gqa_device_errors() == 0
+
+
+PAGED = [
+    # name, B, Hq, Hkv, Smax, dtype, page_size, lens
+    # 64-token pages: the two halves of each 128-token tile come from
+    # different pages (shuffled in the pool)
+    ("mqa_pages64", 3, 64, 1, 640, "bf16", 64, ("list", 640, 129, 1)),
+    ("mqa_pages128_f16", 2, 64, 1, 512, "f16", 128, ("list", 512, 300)),
+    ("g48_pages64_uniform", 4, 96, 2, 384, "bf16", 64, ("uniform",)),
+]
+
+
+@pytest.mark.parametrize("path", [0, 2])
+@pytest.mark.parametrize("case", PAGED, ids=[c[0] for c in PAGED])
+def test_paged_tensor_core_kernel(oracle_mod, case, path):
+    """Paged caches on the tensor-core kernel (page of each 64-token box
+    looked up in the block table): the oracle's output, and the same bits as
+    the contiguous cache."""
+    name, B, Hq, Hkv, Smax, dt, ps, lens = case
+    w = Workload(name, B, Hq, Hkv, 128, Smax, dt, lens=lens,
+                 seed=5200 + PAGED.index(case), page_size=ps)
+    inp = make_inputs(w, pad="nan")
+    ref = oracle_mod.gqa_decode_paged(inp["q"], inp["k"], inp["v"],
+                                      inp["block_table"], inp["seq_lens"],
+                                      inp["scale"])
+    gq.gqa_set_kernel_path(path)
+    out = run_cuda(inp)
+    assert_close(out, ref, f"{name} path {path}")
+    flat = {k: v for k, v in inp.items() if k != "block_table"}
+    flat["k"], flat["v"] = inp["k_contig"], inp["v_contig"]
+    assert torch.equal(run_cuda(flat).view(torch.int16),
+                       out.view(torch.int16))
