@@ -28,13 +28,21 @@ def _limits():
     gq.gqa_set_num_ctas(0)
 
 
-# Units split over several blocks (split combines and their counters), and a
-# ragged 8-bit batch on the narrow-row path.
+# Units split over several blocks (split combines and their counters), a
+# ragged 8-bit batch on the narrow-row path, and the tensor-core kernel.
 CASES = [
     Workload("giveup_bf16_split", 2, 64, 8, 128, 3000, "bf16",
              lens=("list", 3000, 1700), seed=91),
     Workload("giveup_fp8_ragged", 6, 32, 8, 128, 2000, "bf16", kv="e4m3",
              lens=("ragged", 1, 2000), seed=92),
+    # the tensor-core kernel (64 rows per KV head): units split over a
+    # cluster's four blocks and merged through distributed shared memory
+    # (every thread still reaches the cluster barriers after a give-up), and
+    # ragged units split over plain blocks (global split combine)
+    Workload("giveup_mqa_clusters", 8, 64, 1, 128, 512, "bf16",
+             lens=("uniform",), seed=93),
+    Workload("giveup_mqa_split", 2, 64, 1, 128, 1500, "bf16",
+             lens=("list", 1500, 777), seed=94),
 ]
 
 
