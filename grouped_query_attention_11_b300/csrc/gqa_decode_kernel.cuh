@@ -232,9 +232,12 @@ struct Cfg {
                 "the narrow-row path serves 8-bit caches with one head block");
   static_assert(kSTiles % 2 == 0 && kPSteps >= 1, "warp tile shape");
   static_assert(kQSteps % 2 == 0, "QK k-steps are split into two chains");
-  // Short accumulator chains: with few S tiles per warp the QK k-loop is
-  // split over two accumulator sets (even / odd k-steps) and summed.
-  static constexpr bool kSplitQK = kSTiles <= 4;
+  // Short accumulator chains: with two S tiles per warp the QK k-loop is
+  // split over two accumulator sets (even / odd k-steps) and summed.  With
+  // four, the second set's registers push the warp into local-memory spills
+  // at D = 128 (32-row units: 54.3 us split against 50.4 us unsplit on the
+  // 70B shape's 4-token chunk), so those keep one chain per S tile.
+  static constexpr bool kSplitQK = kSTiles <= 2;
 };
 
 __device__ __forceinline__ int clamp_len(int L, int Smax) {
