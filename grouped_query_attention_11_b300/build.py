@@ -66,6 +66,12 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
                         tmp, *objs], check=True)
         os.replace(tmp, LIB)
     finally:
+        # a failed compile leaves the others running: stop them before the
+        # objects they would still write are cleaned up
+        for _, proc in procs:
+            if proc.poll() is None:
+                proc.kill()
+            proc.wait()
         for obj in objs:
             if os.path.exists(obj):
                 os.remove(obj)
