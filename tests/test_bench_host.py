@@ -84,3 +84,27 @@ def test_reference_arm_json_line():
     assert cb["value"] == d["value"]
     assert d["e2e"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_committed_traffic_covers_every_workload_of_these_sources():
+    """The committed ncu summary was taken from the kernel code in the tree
+    (its hash matches) and gives a DRAM figure for every workload bench.py
+    reports, so no line of the bench carries a null traffic; a kernel change
+    without a new capture fails here."""
+    from grouped_query_attention_11_b300.workloads import WORKLOADS
+    missing = [n for n in WORKLOADS if bench.profiled_traffic(n) is None]
+    assert not missing, (
+        "DRAM-traffic summary is stale or incomplete for: " + ", ".join(missing))
+    text = open(os.path.join(ROOT, bench.TRAFFIC_SUMMARY)).read()
+    for name in WORKLOADS:
+        line = next(x for x in text.splitlines()
+                    if f"traffic_bytes_per_launch {name}:" in x)
+        traffic, algo = [int(x) for x in line.split("`") if x.isdigit()]
+        if algo < (1 << 20):
+            # a 67 KB step: fixed per-launch bytes (seq_lens, the error
+            # word, partial sectors) are of the same order as the data
+            continue
+        # one launch moves its algorithmic bytes once, plus the partials and
+        # error words it writes: no re-reads (ncu's counts can fall a little
+        # short where a few lines were still in L2)
+        assert 0.99 * algo <= traffic <= 1.02 * algo, (name, traffic, algo)
