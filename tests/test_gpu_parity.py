@@ -63,6 +63,13 @@ CASES = [
     ("fp8_g16_d128_wide", 2, 32, 2, 128, 300, "bf16", "e4m3",
      ("list", 300, 77)),
     ("e5m2_g12_d64_wide", 2, 24, 2, 64, 200, "f16", "e5m2", ("list", 130, 200)),
+    ("e5m2_g16_d128_wide", 2, 32, 2, 128, 260, "bf16", "e5m2",
+     ("list", 260, 100)),
+    # 8-bit caches with 17..32 rows per unit: two head blocks per warp group
+    ("fp8_g32_d128_two_blocks", 2, 64, 2, 128, 300, "bf16", "e4m3",
+     ("list", 300, 77)),
+    ("e5m2_g24_d64_two_blocks", 2, 48, 2, 64, 200, "f16", "e5m2",
+     ("list", 200, 129)),
     ("fp8_g2_d128_narrow", 3, 8, 4, 128, 333, "bf16", "e4m3",
      ("list", 333, 1, 64)),
     # more sequences than threads per block: the general scheduler prologue
