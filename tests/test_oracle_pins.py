@@ -4,7 +4,8 @@
 * the pages' cache-size figures (closed form);
 * library routines: torch's float16 / bfloat16 / float8_e4m3fn / float8_e5m2
   conversions and
-  torch's scaled_dot_product_attention (``enable_gqa=True``) in float64;
+  torch's scaled_dot_product_attention (``enable_gqa=True``) in float64, on
+  fixed workloads and on random small shapes (hypothesis, derandomized);
 * structural facts the pages state: G = 1 is MHA, GQA equals MHA on a
   repeat_kv-expanded cache, query head h reads KV head floor(h / G), heads that
   share K/V still differ, softmax weights sum to 1;
@@ -19,6 +20,8 @@ import numpy as np
 import pytest
 import torch
 import torch.nn.functional as F
+from hypothesis import HealthCheck, given, settings
+from hypothesis import strategies as st
 
 from grouped_query_attention_11_b300.workloads import (Workload, make_inputs,
                                                        small_variant, WORKLOADS)
@@ -200,6 +203,26 @@ def test_oracle_matches_torch_sdpa_enable_gqa(oracle_mod, w):
     ref = _sdpa_gqa(inp)
     assert not np.isnan(ours).any()
     np.testing.assert_allclose(ours, ref, rtol=0, atol=1e-12)
+
+
+@settings(max_examples=60, deadline=None, derandomize=True,
+          suppress_health_check=[HealthCheck.function_scoped_fixture])
+@given(B=st.integers(1, 3), Hkv=st.sampled_from([1, 2, 3]),
+       G=st.sampled_from([1, 2, 3, 5, 8]), D=st.sampled_from([8, 16, 64, 128]),
+       Smax=st.integers(1, 48), dtype=st.sampled_from(["f16", "bf16"]),
+       kv=st.sampled_from(["same", "e4m3", "e5m2"]), seed=st.integers(0, 999))
+def test_oracle_matches_torch_sdpa_on_random_shapes(oracle_mod, B, Hkv, G, D,
+                                                    Smax, dtype, kv, seed):
+    """Any group size, head dim, cache type and length mix (empty sequences
+    included): the oracle equals torch's SDPA with enable_gqa in float64."""
+    w = Workload("hyp", B, G * Hkv, Hkv, D, Smax, dtype, kv=kv,
+                 lens=("ragged", 0, Smax), seed=seed)
+    inp = make_inputs(w, pad="nan")
+    ours = oracle_mod.gqa_decode(inp["q"], inp["k"], inp["v"], inp["seq_lens"],
+                                 inp["scale"], k_scale=inp["k_scale"],
+                                 v_scale=inp["v_scale"])
+    assert not np.isnan(ours).any()
+    np.testing.assert_allclose(ours, _sdpa_gqa(inp), rtol=0, atol=1e-12)
 
 
 def test_g1_is_per_head_mha(oracle_mod):
